@@ -1,0 +1,222 @@
+/*
+ * svp.h -- C ABI of the packed speculative-verification library (GB300, sm_103a).
+ *
+ * One step of block-diffusion speculative verification, as described in
+ * "DScale: Scaling Block-Diffusion Speculative Decoding with Adaptive Verification"
+ * (SIII-B tile routing, SIII-C Flat-buffer packer, SIII-D graph integration and Prefix
+ * verifier) and the DFlash-Mini-Lab README (anchor + draft suffix, accept the exact
+ * prefix, top-1/top-2 draft-logit margin):
+ *
+ *   N live requests; request i owns packed rows cu_slots[i] .. cu_slots[i+1]-1 of every
+ *   per-row buffer; row cu_slots[i] + j holds candidate j (j = 0 is the anchor), and its
+ *   target logits predict candidate j + 1.  k_i = cu_slots[i+1] - cu_slots[i] lies in
+ *   [0, w] (0 = inactive).  Row j of request i attends to the request's ctx_len[i]
+ *   context tokens and then to its own candidates 0..j (request-local causal mask).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is DEVICE memory owned by the caller, unless it is marked
+ *     "host".  The library never allocates, frees or synchronises; each call is
+ *     enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and reads no
+ *     device value back to the host, so it can be captured in a CUDA graph.
+ *   - Metadata arrays (cu_slots, ctx_len, cu_ctx, block_table, cu_seqlens) are read on
+ *     the device only.  Values that break the contract (cu_slots not non-decreasing,
+ *     k_i > w, cu_slots[n] > m_cap, a context beyond its storage) never cause an
+ *     out-of-bounds access: the affected request is skipped and a bit is set in the
+ *     workspace status word (see svp_read_status).
+ *   - Host-checkable errors (null pointers, head counts, unsupported head_dim or dtype,
+ *     workspace too small, failed launch) are returned synchronously as svp_status and
+ *     nothing is enqueued.
+ *   - Workspaces: query the size, allocate it once, zero it once with
+ *     svp_workspace_init, then reuse it for every later call of the same entry point.
+ *     Kernels leave their counters at zero when they finish.  Calls that share one
+ *     workspace must not overlap on the GPU.
+ *   - Rows of out/lse that belong to no request (rows >= cu_slots[n], padding) are
+ *     never written.
+ *   - Kernels never trap.  Every wait inside a kernel is bounded; on expiry the kernel
+ *     sets SVP_DEV_TIMEOUT in the status word and returns.
+ */
+#ifndef SVP_H_
+#define SVP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SVP_VERSION 1
+
+typedef enum {
+    SVP_OK = 0,
+    SVP_EINVAL = 1,          /* null pointer, negative size, hq % hkv != 0, ...        */
+    SVP_EUNSUPPORTED = 2,    /* head_dim, dtype, page size or tile mode not supported  */
+    SVP_EWORKSPACE = 3,      /* workspace missing or smaller than the queried size     */
+    SVP_ECUDA = 4            /* a CUDA call or kernel launch failed                    */
+} svp_status;
+
+/* Bits of the device status word (svp_read_status). */
+#define SVP_DEV_BAD_SLOTS   0x1   /* cu_slots decreasing, k_i > w, or cu_slots[n] > m_cap */
+#define SVP_DEV_BAD_CONTEXT 0x2   /* ctx_len < 0 or a context beyond its storage          */
+#define SVP_DEV_TIMEOUT     0x4   /* a bounded in-kernel wait expired                    */
+
+typedef enum { SVP_F32 = 0, SVP_BF16 = 1 } svp_dtype;
+
+/* Query-row tile of the verification attention (DScale SIII-B, path-aware tile router). */
+typedef enum {
+    SVP_TILE_AUTO = 0,      /* w <= 16: SHORT, otherwise WIDE                                */
+    SVP_TILE_SHORT = 1,     /* candidate-width tile: the G query heads sharing one KV head
+                               are packed into one tile of G*min(w, 128/G) rows; split-KV   */
+    SVP_TILE_FIXED128 = 2,  /* contrast: one query head per 128-row tile, one block per
+                               (request, head), no split (the prior-art native tile)       */
+    SVP_TILE_WIDE = 3       /* prefill-style 128-row tile of one head, split-KV            */
+} svp_tile_mode;
+
+/* GQA head layout.  Query head h reads KV head h / (hq / hkv). */
+typedef struct {
+    int32_t hq;       /* query heads                                              */
+    int32_t hkv;      /* key/value heads; hq % hkv == 0                           */
+    int32_t d;        /* head_dim: 64, 128 or 256                                  */
+    float scale;      /* softmax scale; 0 selects 1/sqrt(d)                       */
+} svp_heads;
+
+/* Committed-context KV storage of the requests (DScale SIII-D: historyKV). */
+typedef struct {
+    int32_t paged;              /* 0: contiguous varlen, 1: paged                          */
+    const void *k;              /* contiguous: [total_tokens, hkv, d]; paged: page pool   */
+    const void *v;              /* same layout as k                                        */
+    const int64_t *cu_ctx;      /* contiguous: [n] first token row of request i            */
+    int64_t total_tokens;       /* contiguous: rows in k/v (a host-known allocation size) */
+    const int32_t *block_table; /* paged: [n, max_pages] page ids, row-major              */
+    int32_t max_pages;          /* paged: columns of block_table                          */
+    int32_t page_size;          /* paged: tokens per page; must be 16                      */
+    int64_t num_pages;          /* paged: pages in the pool                                */
+    int64_t stride_page;        /* paged: element strides of the pool; the last dim (d)   */
+    int64_t stride_head;        /*   is contiguous.  [pages][hkv][16][d] and              */
+    int64_t stride_tok;         /*   [pages][16][hkv][d] are both expressible.            */
+} svp_kv;
+
+/* Library version and status text. */
+int32_t svp_version(void);
+const char *svp_status_string(svp_status s);
+
+/* Zero a workspace (once, after allocating it).  Enqueued on `stream`. */
+svp_status svp_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Copy the device status word of a workspace into *status (host) and clear it.
+ * This is the one call that synchronises `stream`. */
+svp_status svp_read_status(void *ws, void *stream, int32_t *status);
+
+/* ---------------------------------------------------------------------------------- */
+/* Verification attention over packed, ragged candidate prefixes.                      */
+/* DScale SIII-B (short verify tile sized to the candidate width; grid over requests,   */
+/* heads and query tiles), SIII-C (packed rows, offsets), SIII-D (rows read             */
+/* offset_i + j with request-local causal masking over the supplied KV refs).           */
+
+/* Workspace bytes for svp_verify_attn_packed(_ex) with these sizes (host). */
+svp_status svp_verify_attn_workspace_size(int32_t n, int32_t m_cap, int32_t w,
+                                          const svp_heads *heads, svp_dtype dtype,
+                                          int32_t tile_mode, size_t *bytes);
+
+/*
+ * q      [m_cap, hq, d]   queries of the packed candidate rows
+ * k_new  [m_cap, hkv, d]  keys of the packed candidate rows (same row map as q)
+ * v_new  [m_cap, hkv, d]  values of the packed candidate rows
+ * kv     host struct describing the committed context (contiguous or paged)
+ * ctx_len  [n] int32      context tokens of each request
+ * cu_slots [n+1] int32    packed row offsets (exclusive prefix sums of k_i)
+ * n, m_cap, w             requests, packed row capacity, largest allowed k_i (host)
+ * heads, dtype            host; q/k/v/kv/out share dtype (SVP_F32 or SVP_BF16)
+ * out    [m_cap, hq, d]   softmax(scale q K^T) V per row, in dtype
+ * lse    [m_cap, hq] fp32 natural-log softmax normaliser per row (may be NULL)
+ * ws     workspace of at least svp_verify_attn_workspace_size bytes
+ * dtype SVP_F32 runs an fp32 FFMA kernel; SVP_BF16 runs the tcgen05/TMA kernel with
+ * fp32 accumulation.  All of q, k_new, v_new, kv->k, kv->v, out must be 16-byte aligned.
+ */
+svp_status svp_verify_attn_packed(const void *q, const void *k_new, const void *v_new,
+                                  const svp_kv *kv, const int32_t *ctx_len,
+                                  const int32_t *cu_slots, int32_t n, int32_t m_cap,
+                                  int32_t w, const svp_heads *heads, svp_dtype dtype,
+                                  void *out, float *lse, void *ws, size_t ws_bytes,
+                                  void *stream);
+
+/* As svp_verify_attn_packed, with an explicit svp_tile_mode (SVP_BF16 only for modes
+ * other than AUTO). */
+svp_status svp_verify_attn_packed_ex(const void *q, const void *k_new, const void *v_new,
+                                     const svp_kv *kv, const int32_t *ctx_len,
+                                     const int32_t *cu_slots, int32_t n, int32_t m_cap,
+                                     int32_t w, const svp_heads *heads, svp_dtype dtype,
+                                     int32_t tile_mode, void *out, float *lse, void *ws,
+                                     size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* Wide-tile causal prefill attention (the contrast path of DScale SIII-B: prefill keeps */
+/* the hardware-selected 128-row tile for KV reuse).                                    */
+
+svp_status svp_prefill_attn_workspace_size(int32_t n, int32_t max_s,
+                                           const svp_heads *heads, svp_dtype dtype,
+                                           size_t *bytes);
+
+/*
+ * q [total_s, hq, d], k, v [total_s, hkv, d]  sequences packed by cu_seqlens
+ * cu_seqlens [n+1] int32 (device)  row offsets; sequence lengths <= max_s (host bound)
+ * causal   must be 1
+ * out [total_s, hq, d] (dtype), lse [total_s, hq] fp32 (may be NULL)
+ * SVP_BF16 only.
+ */
+svp_status svp_prefill_attn(const void *q, const void *k, const void *v,
+                            const int32_t *cu_seqlens, int32_t n, int32_t max_s,
+                            int64_t total_s, int32_t causal, const svp_heads *heads,
+                            svp_dtype dtype, void *out, float *lse, void *ws,
+                            size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* Row top-1 / top-2 / margin over vocabulary logits (DFlash-Mini-Lab, DFlash7-ACT     */
+/* margin; DScale SII-B, Fig. 4 Top1-Top2 logit gap).                                  */
+/*   top1_idx = smallest index of the row maximum; top1 = the maximum;                  */
+/*   top2 = second element of the row sorted descending as a multiset (a repeated       */
+/*   maximum gives top2 == top1); margin = top1 - top2 in fp32.  NaN is not supported.   */
+
+svp_status svp_draft_margin_workspace_size(int32_t rows, int32_t vocab, size_t *bytes);
+
+/*
+ * logits [rows, row_stride] (dtype), vocab <= row_stride, vocab >= 2; rows may be 0.
+ * Outputs [rows] each; any output pointer may be NULL.
+ */
+svp_status svp_draft_margin(const void *logits, int64_t row_stride, int32_t rows,
+                            int32_t vocab, svp_dtype dtype, int32_t *top1_idx,
+                            float *top1, float *top2, float *margin, void *ws,
+                            size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* Greedy prefix acceptance (DScale SIII-D, Prefix verifier at temperature 0;           */
+/* DFlash-Mini-Lab "accept exact prefix").                                              */
+/*   a_i = largest a <= k_i - 1 with tokens[off_i + j] == target_argmax[off_i + j - 1]   */
+/*   for all 1 <= j <= a; accept_len[i] = 1 + a_i (the anchor counts);                   */
+/*   next_token[i] = target_argmax[off_i + a_i] (row off_i + a_i supplies the successor).*/
+/*   k_i = 0: accept_len = 0, next_token = -1.                                          */
+
+/*
+ * target_argmax [m_cap] int32, tokens [m_cap] int32 (row off_i = anchor, off_i + j =
+ * draft j), cu_slots [n+1]; outputs accept_len [n], next_token [n].  No workspace.
+ */
+svp_status svp_greedy_accept(const int32_t *target_argmax, const int32_t *tokens,
+                             const int32_t *cu_slots, int32_t n, int32_t m_cap,
+                             int32_t *accept_len, int32_t *next_token, void *stream);
+
+/* Fused: svp_draft_margin over the packed target-logit rows, then svp_greedy_accept,
+ * in one launch.  Rows >= cu_slots[n] are not read.  m_cap rows of logits. */
+svp_status svp_margin_accept_workspace_size(int32_t n, int32_t m_cap, int32_t vocab,
+                                            size_t *bytes);
+
+svp_status svp_margin_accept(const void *logits, int64_t row_stride, int32_t m_cap,
+                             int32_t vocab, svp_dtype dtype, const int32_t *tokens,
+                             const int32_t *cu_slots, int32_t n, int32_t *top1_idx,
+                             float *top1, float *top2, float *margin, int32_t *accept_len,
+                             int32_t *next_token, void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVP_H_ */

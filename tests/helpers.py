@@ -1,0 +1,78 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the binding and
+the fp64 oracle on the same seeded batch, and compare."""
+import numpy as np
+import torch
+
+import oracle
+import speculative_decoding_verification_packed_gb300 as svp
+
+BF16_MAX_ABS = 2e-2     # attention bars for bf16 inputs with fp32 accumulation
+BF16_MEAN_ABS = 2e-3
+F32_MAX_ABS = 1e-4      # attention bar for fp32 inputs
+
+
+def to_dev(b, device="cuda"):
+    """Copy every tensor field of a workloads.Batch to the device (new object)."""
+    import copy
+    d = copy.copy(b)
+    for name, val in vars(b).items():
+        if isinstance(val, torch.Tensor):
+            setattr(d, name, val.to(device))
+    d.full = {}
+    return d
+
+
+def gpu_verify(bd, tile_mode=svp.TILE_AUTO, w=None, out=None, lse=None):
+    kw = {}
+    if bd.paged:
+        kw = dict(k_cache=bd.k_cache, v_cache=bd.v_cache, block_table=bd.block_table)
+    else:
+        kw = dict(k_ctx=bd.k_ctx, v_ctx=bd.v_ctx, cu_ctx=bd.cu_ctx)
+    out, lse = svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots,
+                                      w=w or bd.W, tile_mode=tile_mode, out=out, lse=lse, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_verify(b, requests=None, threads=16):
+    """b: CPU batch."""
+    if b.paged:
+        return oracle.attention(b.q, b.k_new, b.v_new, b.ctx_len, b.cu_slots, hkv=b.hkv,
+                                scale=b.scale, k_cache=b.k_cache, v_cache=b.v_cache,
+                                block_table=b.block_table, cache_strides=b.cache_strides,
+                                requests=requests, threads=threads)
+    return oracle.attention(b.q, b.k_new, b.v_new, b.ctx_len, b.cu_slots, hkv=b.hkv,
+                            scale=b.scale, k_ctx=b.k_ctx, v_ctx=b.v_ctx, cu_ctx=b.cu_ctx,
+                            requests=requests, threads=threads)
+
+
+def rows_of(b, requests=None):
+    cu = b.cu_slots.tolist()
+    reqs = range(b.n) if requests is None else requests
+    rows = []
+    for i in reqs:
+        rows.extend(range(cu[i], cu[i + 1]))
+    return np.array(rows, dtype=np.int64)
+
+
+def compare_attention(out_gpu, lse_gpu, ref_o, ref_l, rows, dtype):
+    """Element-wise comparison on the given packed rows; returns error stats."""
+    o = out_gpu.float().cpu().numpy()[rows]
+    r = ref_o[rows]
+    err = np.abs(o.astype(np.float64) - r)
+    stats = dict(max_abs=float(err.max()), mean_abs=float(err.mean()),
+                 max_rel=float((err / np.maximum(np.abs(r), 1e-3)).max()))
+    if lse_gpu is not None:
+        le = np.abs(lse_gpu.cpu().numpy()[rows].astype(np.float64) - ref_l[rows])
+        stats["lse_max_abs"] = float(le.max())
+    if dtype == torch.float32:
+        assert stats["max_abs"] <= F32_MAX_ABS, stats
+        if lse_gpu is not None:
+            assert stats["lse_max_abs"] <= F32_MAX_ABS, stats
+    else:
+        assert stats["max_abs"] <= BF16_MAX_ABS, stats
+        assert stats["mean_abs"] <= BF16_MEAN_ABS, stats
+        if lse_gpu is not None:
+            assert stats["lse_max_abs"] <= 1e-3, stats
+    assert np.isfinite(o).all()
+    return stats

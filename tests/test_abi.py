@@ -1,0 +1,84 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads, exports
+every function include/svp.h declares, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_packed_gb300 as svp
+from speculative_decoding_verification_packed_gb300 import build as svp_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    svp_build.build()
+    return svp.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "svp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(svp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert "svp_verify_attn_packed" in names and "svp_margin_accept" in names
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    assert L.svp_version() == 1
+    assert svp.status_string(svp.SVP_OK) == "ok"
+    assert "workspace" in svp.status_string(svp.SVP_EWORKSPACE)
+
+
+def test_workspace_size_queries():
+    a = svp.verify_attn_workspace_size(8, 128, 16, 32, 8, 128)
+    b = svp.verify_attn_workspace_size(64, 512, 16, 32, 8, 128)
+    assert 0 < a <= b
+    assert svp.verify_attn_workspace_size(3, 24, 16, 4, 2, 64, dtype=__import__("torch").float32) >= 256
+    assert svp.draft_margin_workspace_size(224, 248320) > 224 * 16 * 12
+    assert svp.margin_accept_workspace_size(32, 224, 248320) >= svp.draft_margin_workspace_size(224, 248320)
+    assert svp.prefill_attn_workspace_size(1, 4096, 32, 8, 128) > 0
+
+
+def test_invalid_arguments_rejected_on_host(L):
+    h = svp.svp_heads(32, 7, 128, 0.0)      # hq % hkv != 0
+    out = ctypes.c_size_t(0)
+    assert L.svp_verify_attn_workspace_size(8, 128, 16, ctypes.byref(h), 1, 0,
+                                            ctypes.byref(out)) == svp.SVP_EINVAL
+    h = svp.svp_heads(32, 8, 96, 0.0)       # unsupported head_dim
+    assert L.svp_verify_attn_workspace_size(8, 128, 16, ctypes.byref(h), 1, 0,
+                                            ctypes.byref(out)) == svp.SVP_EUNSUPPORTED
+    h = svp.svp_heads(32, 8, 128, 0.0)
+    kv = svp.svp_kv()
+    # missing workspace
+    assert L.svp_verify_attn_packed(1, 1, 1, ctypes.byref(kv), 1, 1, 8, 128, 16, ctypes.byref(h),
+                                    1, 1, None, None, 0, None) == svp.SVP_EWORKSPACE
+    # null q with a workspace
+    assert L.svp_verify_attn_packed(None, 1, 1, ctypes.byref(kv), 1, 1, 8, 128, 16,
+                                    ctypes.byref(h), 1, 1, None, 1, 1 << 30, None) == svp.SVP_EINVAL
+    # vocab < 2
+    assert L.svp_draft_margin(1, 1, 4, 1, 1, None, None, None, None, 1, 1 << 20,
+                              None) == svp.SVP_EINVAL
+    # prefill without causal
+    assert L.svp_prefill_attn(1, 1, 1, 1, 1, 16, 16, 0, ctypes.byref(h), 1, 1, None, 1, 1 << 20,
+                              None) == svp.SVP_EUNSUPPORTED
+    # empty batch is a no-op
+    assert L.svp_verify_attn_packed(None, None, None, ctypes.byref(kv), None, None, 0, 0, 16,
+                                    ctypes.byref(h), 1, None, None, 1, 1 << 20, None) == svp.SVP_OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(4, 2, 64)
+    with pytest.raises((ValueError, RuntimeError)):
+        svp.verify_attn_packed(q, q[:, :1], q[:, :1], torch.zeros(1, dtype=torch.int32),
+                               torch.tensor([0, 4], dtype=torch.int32), w=16,
+                               k_ctx=q[:0, :1], v_ctx=q[:0, :1],
+                               cu_ctx=torch.zeros(2, dtype=torch.int64))

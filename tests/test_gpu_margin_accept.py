@@ -1,0 +1,149 @@
+"""GPU parity: row top-1/top-2/margin and greedy acceptance vs the oracle (bit-exact).
+
+Accept lengths, next tokens and argmax indices must match exactly; top-1/top-2 values
+and the fp32 margin are compared bit for bit (same input values, same fp32 subtraction).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_packed_gb300 as svp
+from speculative_decoding_verification_packed_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(a):
+    return np.asarray(a, dtype=np.float32).view(np.int32)
+
+
+def _check_rows(logits_cpu, outs, rows=None):
+    idx, t1, t2, mg = (o.cpu().numpy() for o in outs[:4])
+    r_idx, r_t1, r_t2, r_mg = oracle.row_top2(logits_cpu)
+    sel = slice(None) if rows is None else rows
+    assert np.array_equal(idx[sel], r_idx[sel])
+    assert np.array_equal(_bits(t1[sel]), _bits(r_t1[sel]))
+    assert np.array_equal(_bits(t2[sel]), _bits(r_t2[sel]))
+    ok = (_bits(mg[sel]) == _bits(r_mg[sel])) | (np.isnan(mg[sel]) & np.isnan(r_mg[sel]))
+    assert ok.all()
+    return r_idx
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("vocab", [2, 7, 512, 40000, 248320])
+def test_draft_margin_random_rows(dtype, vocab):
+    g = torch.Generator().manual_seed(vocab)
+    x = (torch.randn(37, vocab, generator=g) * 2).to(dtype)
+    x[1, :] = 3.0                                  # all equal: idx 0, margin 0
+    x[2, vocab - 1] = 100.0                        # max at the last index
+    x[3, 0] = 100.0; x[3, vocab - 1] = 100.0      # tie at both ends
+    x[4, :] = float("-inf"); x[4, vocab // 2] = -5.0
+    x[5, :] = float("-inf")                        # all -inf: margin NaN
+    outs = svp.draft_margin(x.cuda())
+    torch.cuda.synchronize()
+    _check_rows(x, outs)
+
+
+def test_draft_margin_strided_and_unaligned_rows():
+    import ctypes
+    g = torch.Generator().manual_seed(1)
+    base = torch.randn(20, 1003, generator=g).to(torch.bfloat16)
+    dev = base.cuda()
+    n_rows, vocab = 20, 1000
+    outs = [torch.empty(n_rows, dtype=torch.int32, device="cuda")] + \
+           [torch.empty(n_rows, dtype=torch.float32, device="cuda") for _ in range(3)]
+    ws = svp.Workspace(svp.draft_margin_workspace_size(n_rows, vocab))
+    # rows start 2 bytes past a 16-byte boundary, row stride 1003 > vocab
+    st = svp.lib().svp_draft_margin(ctypes.c_void_p(dev.data_ptr() + 2), 1003, n_rows, vocab,
+                                    svp.SVP_BF16, outs[0].data_ptr(), outs[1].data_ptr(),
+                                    outs[2].data_ptr(), outs[3].data_ptr(), ws.ptr, ws.nbytes,
+                                    torch.cuda.current_stream().cuda_stream)
+    assert st == svp.SVP_OK
+    torch.cuda.synchronize()
+    _check_rows(base[:, 1:1001].contiguous(), outs)
+    # aligned rows with padding beyond the vocabulary
+    padded = torch.zeros(20, 1008, dtype=torch.bfloat16)
+    padded[:, :1000] = base[:, :1000]
+    padded[:, 1000:] = 1000.0                      # must be ignored
+    outs = svp.draft_margin(padded.cuda(), vocab=1000)
+    torch.cuda.synchronize()
+    _check_rows(base[:, :1000].contiguous(), outs)
+
+
+def test_margin_accept_tiny_fp32():
+    b = wl.make_batch("tiny_fp32", seed=0, poison=True)
+    outs = svp.margin_accept(b.target_logits.cuda(), b.tokens.cuda(), b.cu_slots.cuda())
+    torch.cuda.synchronize()
+    rows = np.arange(b.m_live)
+    r_idx = _check_rows(b.target_logits[:b.m_live], [o[:b.m_live] for o in outs[:4]])
+    acc, nxt = oracle.greedy_accept(np.concatenate([r_idx, np.zeros(b.m_cap - b.m_live, np.int32)]),
+                                    b.tokens, b.cu_slots)
+    assert np.array_equal(outs[4].cpu().numpy(), acc)
+    assert np.array_equal(outs[5].cpu().numpy(), nxt)
+
+
+def test_margin_accept_wide_vocab_workload():
+    b = wl.make_batch("wide_gqa_bf16", seed=0, hq=2, hkv=1, d=64, ctx_lengths=[0] * 32)
+    outs = svp.margin_accept(b.target_logits.cuda(), b.tokens.cuda(), b.cu_slots.cuda())
+    torch.cuda.synchronize()
+    r_idx = _check_rows(b.target_logits, outs)
+    acc, nxt = oracle.greedy_accept(r_idx, b.tokens, b.cu_slots)
+    assert np.array_equal(outs[4].cpu().numpy(), acc)
+    assert np.array_equal(outs[5].cpu().numpy(), nxt)
+    assert (outs[4].cpu().numpy() <= 7).all() and (outs[4].cpu().numpy() >= 1).all()
+    # draft-side margins over the draft logits
+    d = svp.draft_margin(b.draft_logits.cuda())
+    torch.cuda.synchronize()
+    _check_rows(b.draft_logits, d)
+
+
+def test_margin_accept_inactive_and_tail_not_read():
+    V = 1000
+    g = torch.Generator().manual_seed(3)
+    cu = torch.tensor([0, 3, 3, 8, 8], dtype=torch.int32)      # requests 1 and 3 inactive
+    m_cap = 12
+    logits = torch.randn(m_cap, V, generator=g)
+    logits[8:] = float("nan")                                   # tail: must not be read
+    argmax = logits[:8].argmax(-1).to(torch.int32)
+    tokens = torch.randint(0, V, (m_cap,), generator=g, dtype=torch.int32)
+    tokens[1] = argmax[0]; tokens[2] = argmax[1]               # request 0: full accept
+    tokens[4] = argmax[3]                                       # request 2: accept 1 draft
+    outs = svp.margin_accept(logits.cuda(), tokens.cuda(), cu.cuda())
+    torch.cuda.synchronize()
+    r_idx = _check_rows(logits[:8], [o[:8] for o in outs[:4]])
+    acc, nxt = oracle.greedy_accept(np.concatenate([r_idx, np.zeros(4, np.int32)]), tokens, cu)
+    assert outs[4].cpu().tolist() == acc.tolist() == [3, 0, 2, 0]
+    assert outs[5].cpu().tolist() == nxt.tolist()
+    assert outs[5].cpu().tolist()[1] == -1
+    assert (outs[0][8:].cpu() == -1).all()                      # tail rows untouched
+
+
+def test_greedy_accept_all_patterns():
+    rng = np.random.default_rng(0)
+    k = 8
+    import itertools
+    pats = list(itertools.product([False, True], repeat=k - 1))
+    n = len(pats)
+    cu = (np.arange(n + 1) * k).astype(np.int32)
+    argmax = rng.integers(0, 1000, size=n * k).astype(np.int32)
+    tokens = rng.integers(0, 1000, size=n * k).astype(np.int32)
+    for i, p in enumerate(pats):
+        for j in range(1, k):
+            tgt = argmax[i * k + j - 1]
+            tokens[i * k + j] = tgt if p[j - 1] else (tgt + 1) % 1000
+    acc, nxt = svp.greedy_accept(torch.from_numpy(argmax).cuda(), torch.from_numpy(tokens).cuda(),
+                                 torch.from_numpy(cu).cuda())
+    r_acc, r_nxt = oracle.greedy_accept(argmax, tokens, cu)
+    assert np.array_equal(acc.cpu().numpy(), r_acc)
+    assert np.array_equal(nxt.cpu().numpy(), r_nxt)
+
+
+def test_repeated_margin_calls_reuse_workspace():
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(50, 30000, generator=g).to(torch.bfloat16).cuda()
+    a = svp.draft_margin(x)
+    b = svp.draft_margin(x)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
