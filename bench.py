@@ -1,0 +1,560 @@
+#!/usr/bin/env python
+"""Benchmark of one packed speculative-verification step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the hot path over one batch of the workload:
+  * full_width_bf16 (default), budget8n_bf16, paged_n64_bf16: verification attention
+    (tile router -> split-KV work decomposition -> GQA-packed short tile -> online
+    softmax -> PV -> combine), one launch;
+  * wide_gqa_bf16: verification attention, draft-logit margin and the fused target
+    margin + greedy acceptance (three launches).
+The metric is verified candidate rows per second (rows = packed live rows M_live).
+Inputs are resident in HBM when the timed region starts; consecutive steps rotate over
+several independent input sets whose total footprint exceeds twice the L2 size, so a
+step never finds its KV stream in L2.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this repository) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "verified candidate rows/s and KV-stream HBM GB/s (% of GB300 peak) at N, budget"
+NOMINAL_HBM_GBS = 8000.0
+
+WORKLOAD_TEXT = {
+    "full_width_bf16": "N=8 requests x 16 slots (128 packed rows), 32q/8kv heads, d=128, "
+                       "contiguous KV context ~U[512,8192], bf16",
+    "budget8n_bf16": "N=8 requests, shared budget 64 slots (8N), truncated-geometric "
+                     "lengths, 32q/8kv, d=128, contiguous KV ~U[512,8192], bf16",
+    "paged_n64_bf16": "N=64 requests, budget 512 slots (8N), 32q/8kv, d=128, paged KV "
+                      "(16-token pages, shuffled block table) ~U[4096,32768], bf16",
+    "wide_gqa_bf16": "N=32 x 7 slots (224 rows), 24q/2kv, d=256, KV ~U[1024,8192], plus "
+                     "draft margin over [192,248320] and fused margin+greedy accept over "
+                     "target logits [224,248320], bf16",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="full_width_bf16", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the contrast / other-workload measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max over ranks of a host float (timing plumbing only, not a data-path exchange)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ours
+def kv_bytes(b) -> int:
+    """Algorithmic KV bytes of one attention launch: every context and candidate token's
+    K and V row of each KV head is read once."""
+    L = int(b.ctx_len.sum().item())
+    k = int(b.cu_slots[-1].item())
+    return (L + k) * b.hkv * b.d * 2 * b.q.element_size()
+
+
+def attn_kwargs(b):
+    if b.paged:
+        return dict(k_cache=b.k_cache, v_cache=b.v_cache, block_table=b.block_table)
+    return dict(k_ctx=b.k_ctx, v_ctx=b.v_ctx, cu_ctx=b.cu_ctx)
+
+
+def build_step(b, svp, tile_mode=None):
+    """Returns (launch list of (name, fn)), outputs preallocated; fixed workspaces."""
+    import torch
+    mode = svp.TILE_AUTO if tile_mode is None else tile_mode
+    out = torch.empty_like(b.q)
+    lse = torch.empty((b.m_cap, b.hq), dtype=torch.float32, device=b.q.device)
+    kv = svp.make_kv(**attn_kwargs(b))
+    ws = svp.Workspace(svp.verify_attn_workspace_size(b.n, b.m_cap, b.W, b.hq, b.hkv, b.d,
+                                                      b.dtype, mode))
+
+    def attn():
+        svp.verify_attn_packed(b.q, b.k_new, b.v_new, b.ctx_len, b.cu_slots, w=b.W, kv=kv,
+                               out=out, lse=lse, tile_mode=mode, ws=ws)
+
+    launches = [("attn", attn)]
+    if b.target_logits is not None and b.draft_logits is not None:
+        V = b.target_logits.shape[1]
+        dev = b.q.device
+        rows_d = b.draft_logits.shape[0]
+        d_outs = (torch.empty(rows_d, dtype=torch.int32, device=dev),) + tuple(
+            torch.empty(rows_d, dtype=torch.float32, device=dev) for _ in range(3))
+        ws_d = svp.Workspace(svp.draft_margin_workspace_size(rows_d, V))
+        t_outs = (torch.empty(b.m_cap, dtype=torch.int32, device=dev),) + tuple(
+            torch.empty(b.m_cap, dtype=torch.float32, device=dev) for _ in range(3)) + (
+            torch.empty(b.n, dtype=torch.int32, device=dev),
+            torch.empty(b.n, dtype=torch.int32, device=dev))
+        ws_t = svp.Workspace(svp.margin_accept_workspace_size(b.n, b.m_cap, V))
+
+        def draft():
+            svp.draft_margin(b.draft_logits, ws=ws_d, outs=d_outs)
+
+        def accept():
+            svp.margin_accept(b.target_logits, b.tokens, b.cu_slots, ws=ws_t, outs=t_outs)
+
+        launches += [("draft_margin", draft), ("margin_accept", accept)]
+    return launches, (out, lse)
+
+
+def step_bytes(b):
+    kvb = kv_bytes(b)
+    logit = 0
+    if b.target_logits is not None and b.draft_logits is not None:
+        logit = (b.m_live * b.target_logits.shape[1] + b.draft_logits.numel()) * 2
+    return kvb, logit
+
+
+def make_sets(name, nsets, seed, device):
+    from speculative_decoding_verification_packed_gb300 import workloads as wl
+    return [wl.make_batch(name, seed=seed + s, device=device) for s in range(nsets)]
+
+
+def n_sets_for(b0) -> int:
+    kvb, lg = step_bytes(b0)
+    per = kvb + lg + 1
+    return max(1, min(8, math.ceil(2 * L2_BYTES / per) + 1)) if per < 4 * L2_BYTES else 1
+
+
+def timed_run(sets, steps, warmup, svp, tile_mode=None, clocks=None):
+    """K steps rotating over the input sets; per-launch device times via events."""
+    import torch
+    plans = [build_step(b, svp, tile_mode)[0] for b in sets]
+    stream = torch.cuda.current_stream()
+    for w in range(warmup):
+        for _, fn in plans[w % len(plans)]:
+            fn()
+    torch.cuda.synchronize()
+    nl = len(plans[0])
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nl)] for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    t0.record(stream)
+    for s in range(steps):
+        for li, (_, fn) in enumerate(plans[s % len(plans)]):
+            ev[s][li][0].record(stream)
+            fn()
+            ev[s][li][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop() if clocks else None
+    total_ms = t0.elapsed_time(t1)
+    per_launch = [statistics.mean(ev[s][li][0].elapsed_time(ev[s][li][1]) for s in range(steps))
+                  for li in range(nl)]
+    names = [n for n, _ in plans[0]]
+    return total_ms, dict(zip(names, per_launch)), clk, wall, steps * nl
+
+
+def e2e_run(sets, steps, warmup, svp):
+    """Same step through the public API with host (pinned) inputs: every step copies its
+    inputs host->device, runs the step, and reads the outputs back."""
+    import torch
+    hosts = []
+    for b in sets:
+        h = {}
+        for name in ("q", "k_new", "v_new", "ctx_len", "cu_slots", "k_ctx", "v_ctx", "cu_ctx",
+                     "k_cache", "v_cache", "block_table", "tokens", "target_logits",
+                     "draft_logits"):
+            t = getattr(b, name)
+            if t is not None:
+                h[name] = t.cpu().pin_memory()
+        hosts.append(h)
+    b0 = sets[0]
+    plan, (out, lse) = build_step(b0, svp)
+    h2d = sum(t.numel() * t.element_size() for t in hosts[0].values())
+    d2h_host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d2h_host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one(s):
+        h = hosts[s % len(hosts)]
+        for name, t in h.items():
+            getattr(b0, name).copy_(t, non_blocking=True)
+        for _, fn in plan:
+            fn()
+        d2h_host_out.copy_(out, non_blocking=True)
+        d2h_host_lse.copy_(lse, non_blocking=True)
+
+    for w in range(warmup):
+        one(w)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(steps):
+        one(s)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+def traffic_record(workload: str):
+    """ncu DRAM bytes per launch of the attention kernel from profiles/, if the kernel
+    source is unchanged since the capture (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    src = os.path.join(ROOT, "speculative_decoding_verification_packed_gb300", "csrc", "attn_tc.cu")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    r = rec.get(workload)
+    if not r or r.get("attn_tc_sha") != h:
+        return None
+    return r.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(name, seed, budget_s=15.0):
+    """The fp64 oracle timed on this host's cores on a bounded sample of the workload."""
+    import torch
+    import oracle
+    from speculative_decoding_verification_packed_gb300 import workloads as wl
+    threads = os.cpu_count() or 1
+    b = wl.make_batch(name, seed=seed, device="cpu", with_logits=False)
+    cu = b.cu_slots.tolist()
+    order = list(range(b.n))
+    done_rows, t_used, reqs = 0, 0.0, []
+    for i in order:
+        t0 = time.perf_counter()
+        if b.paged:
+            oracle.attention(b.q, b.k_new, b.v_new, b.ctx_len, b.cu_slots, hkv=b.hkv, scale=b.scale,
+                             k_cache=b.k_cache, v_cache=b.v_cache, block_table=b.block_table,
+                             cache_strides=b.cache_strides, requests=[i], threads=threads)
+        else:
+            oracle.attention(b.q, b.k_new, b.v_new, b.ctx_len, b.cu_slots, hkv=b.hkv, scale=b.scale,
+                             k_ctx=b.k_ctx, v_ctx=b.v_ctx, cu_ctx=b.cu_ctx, requests=[i],
+                             threads=threads)
+        t_used += time.perf_counter() - t0
+        done_rows += cu[i + 1] - cu[i]
+        reqs.append(i)
+        if t_used >= budget_s:
+            break
+    return {"value": done_rows / t_used, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(reqs)} of {b.n} requests ({done_rows} rows, all heads) of {name}, "
+                      f"seed {seed}, fp64 C oracle, {t_used:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    import speculative_decoding_verification_packed_gb300 as svp
+    from speculative_decoding_verification_packed_gb300 import build as svp_build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(svp.LIB_PATH):
+        svp_build.build()
+    barrier(world)
+    hbm_peak, tf_peak, peak_kind = measured_peaks()
+    dev = torch.device("cuda", local)
+
+    # the headline workload; each rank runs its own batch (weak scaling, no exchange)
+    probe = make_sets(args.workload, 1, args.seed + 1000 * rank, dev)
+    nsets = n_sets_for(probe[0])
+    sets = probe + make_sets(args.workload, nsets - 1, args.seed + 1000 * rank + 1, dev)
+    clocks = ClockSampler(local)
+    barrier(world)
+    total_ms, per_launch, clk, wall, launches = timed_run(sets, args.steps, args.warmup, svp,
+                                                          clocks=clocks)
+    total_ms = reduce_max(total_ms, world)
+    rows = reduce_sum(sum(int(sets[s % nsets].cu_slots[-1]) for s in range(args.steps)), world)
+    ms_step = total_ms / args.steps
+    value = rows / (total_ms / 1e3)
+    kvb = statistics.mean(kv_bytes(b) for b in sets)
+    attn_ms = per_launch["attn"]
+    achieved = kvb / (attn_ms / 1e3) / 1e9
+    tr = traffic_record(args.workload)
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; sizes and distributions of the workload)",
+        "config": {"workload": args.workload, "description": WORKLOAD_TEXT[args.workload],
+                   "n_requests": sets[0].n, "budget_slots": sets[0].m_cap,
+                   "live_rows": int(sets[0].cu_slots[-1]),
+                   "l2": f"{nsets} rotating input sets, {nsets * (kvb / 1e6):.0f} MB of KV "
+                         f"(> 2x the 129 MB L2)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": tr, "kernel": "attn_tc_kernel",
+                     "algorithmic_bytes_per_launch": int(kvb), "launch_us": round(attn_ms * 1e3, 2),
+                     "peak_kind": peak_kind,
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
+        "kv_gbs": round(achieved, 1),
+        "per_launch_us": {k: round(v * 1e3, 2) for k, v in per_launch.items()},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if "draft_margin" in per_launch:
+        V = sets[0].target_logits.shape[1]
+        lb = sets[0].draft_logits.numel() * 2
+        result["draft_margin_gbs"] = round(lb / (per_launch["draft_margin"] / 1e3) / 1e9, 1)
+        tb = int(sets[0].cu_slots[-1]) * V * 2
+        result["margin_accept_gbs"] = round(tb / (per_launch["margin_accept"] / 1e3) / 1e9, 1)
+
+    # end to end through the public API with host buffers
+    e2e_ms, h2d, d2h = e2e_run(sets[:2], max(3, args.steps // 5), 3, svp)
+    e2e_steps = max(3, args.steps // 5)
+    e2e_rows = sum(int(sets[s % 2].cu_slots[-1]) for s in range(e2e_steps)) if nsets > 1 else \
+        e2e_steps * int(sets[0].cu_slots[-1])
+    result["e2e"] = {"value": round(e2e_rows / (e2e_ms / 1e3), 1), "unit": "rows/s",
+                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                     "note": "all step inputs (incl. the KV context) copied from pinned host "
+                             "memory every step"}
+
+    if not args.no_extras and rank == 0:
+        extras = {}
+        # contrast: fixed 128-row tile, same inputs, same N
+        fx_ms, fx_pl, _, _, _ = timed_run(sets, max(5, args.steps // 2), 3, svp,
+                                          tile_mode=svp.TILE_FIXED128)
+        fx_rows = sum(int(sets[s % nsets].cu_slots[-1]) for s in range(max(5, args.steps // 2)))
+        extras["fixed128_contrast"] = {
+            "rows_per_s": round(fx_rows / (fx_ms / 1e3), 1),
+            "kv_gbs": round(kvb / (fx_pl["attn"] / 1e3) / 1e9, 1),
+            "short_tile_speedup": round(value / (fx_rows / (fx_ms / 1e3)), 3)}
+        for other in ("budget8n_bf16", "paged_n64_bf16", "wide_gqa_bf16"):
+            if other == args.workload:
+                continue
+            osets = make_sets(other, 1, args.seed, dev)
+            n2 = n_sets_for(osets[0])
+            osets += make_sets(other, n2 - 1, args.seed + 1, dev)
+            st = max(5, args.steps // 5)
+            oms, opl, _, _, _ = timed_run(osets, st, 3, svp)
+            orows = sum(int(osets[s % n2].cu_slots[-1]) for s in range(st))
+            okv = statistics.mean(kv_bytes(b) for b in osets)
+            e = {"rows_per_s": round(orows / (oms / 1e3), 1),
+                 "kv_gbs": round(okv / (opl["attn"] / 1e3) / 1e9, 1),
+                 "kv_frac": round(okv / (opl["attn"] / 1e3) / 1e9 / hbm_peak, 4),
+                 "per_launch_us": {k: round(v * 1e3, 2) for k, v in opl.items()}}
+            fms, fpl, _, _, _ = timed_run(osets, st, 3, svp, tile_mode=svp.TILE_FIXED128)
+            e["fixed128_rows_per_s"] = round(orows / (fms / 1e3), 1)
+            if "draft_margin" in opl:
+                V = osets[0].target_logits.shape[1]
+                e["draft_margin_gbs"] = round(osets[0].draft_logits.numel() * 2 /
+                                              (opl["draft_margin"] / 1e3) / 1e9, 1)
+                e["margin_accept_gbs"] = round(int(osets[0].cu_slots[-1]) * V * 2 /
+                                               (opl["margin_accept"] / 1e3) / 1e9, 1)
+            extras[other] = e
+            del osets
+            torch.cuda.empty_cache()
+        # wide-tile prefill contrast: tensor-bound
+        from speculative_decoding_verification_packed_gb300 import workloads as wl
+        q, k, v = wl.make_prefill(device=dev)
+        cu = torch.tensor([0, 4096], dtype=torch.int32, device=dev)
+        pout = torch.empty_like(q)
+        plse = torch.empty((4096, 32), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            svp.prefill_attn(q, k, v, cu, max_s=4096, out=pout, lse=plse)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            svp.prefill_attn(q, k, v, cu, max_s=4096, out=pout, lse=plse)
+        e1.record()
+        torch.cuda.synchronize()
+        pms = e0.elapsed_time(e1) / 10
+        flops = 4.0 * 32 * 128 * (4096 * 4097 / 2)
+        extras["prefill_4096_causal"] = {"us": round(pms * 1e3, 1),
+                                         "tflops": round(flops / (pms / 1e3) / 1e12, 1),
+                                         "frac_of_bf16_peak": round(flops / (pms / 1e3) / 1e12 / tf_peak, 4)}
+        result["extras"] = extras
+
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+    elif not args.no_cpu_baseline and rank == 0:
+        result["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle, one bounded sample per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from speculative_decoding_verification_packed_gb300 import workloads as wl
+    oracle.build()
+    threads = os.cpu_count() or 1
+    b = wl.make_batch(args.workload, seed=args.seed, device="cpu", with_logits=False)
+    cu = b.cu_slots.tolist()
+    kw = (dict(k_cache=b.k_cache, v_cache=b.v_cache, block_table=b.block_table,
+               cache_strides=b.cache_strides) if b.paged else
+          dict(k_ctx=b.k_ctx, v_ctx=b.v_ctx, cu_ctx=b.cu_ctx))
+
+    # one step = the request with the shortest context (a bounded sample of the batch)
+    i = min(range(b.n), key=lambda j: (int(b.ctx_len[j]), j))
+
+    def step():
+        oracle.attention(b.q, b.k_new, b.v_new, b.ctx_len, b.cu_slots, hkv=b.hkv, scale=b.scale,
+                         requests=[i], threads=threads, **kw)
+        return cu[i + 1] - cu[i]
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    rows = 0
+    for _ in range(args.steps):
+        rows += step()
+    dt = time.perf_counter() - t0
+    value = rows / dt
+    sample = (f"per step: request {i} of {args.workload} (ctx {int(b.ctx_len[i])}, "
+              f"{cu[i + 1] - cu[i]} rows, all {b.hq} heads), fp64 C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "description": WORKLOAD_TEXT[args.workload]},
+        "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -270,11 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
     sh.total = sh.prefix[NQ];
 
-    // This CTA's unit range.
+    // This CTA's unit range.  The units are cut into ncta = min(grid, units) ranges so
+    // that every range is non-empty (a pair's pieces are then consecutive CTAs).
+    const int32_t ncta = (int32_t)((int64_t)gridDim.x < sh.total ? (int64_t)gridDim.x : sh.total);
     int64_t cta_s, cta_e;
     if (p.split) {
-        cta_s = cta_start(sh.total, blockIdx.x, gridDim.x);
-        cta_e = cta_start(sh.total, blockIdx.x + 1, gridDim.x);
+        if ((int32_t)blockIdx.x < ncta) {
+            cta_s = cta_start(sh.total, blockIdx.x, ncta);
+            cta_e = cta_start(sh.total, blockIdx.x + 1, ncta);
+        } else {
+            cta_s = cta_e = 0;
+        }
     } else {
         // one (request, row block, head group) pair per CTA
         const int32_t pair = blockIdx.x;
@@ -639,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 __threadfence();
                 named_bar_sync(1, 128);
                 if (stid == 0) {
-                    const int32_t C0 = gridDim.x;
+                    const int32_t C0 = ncta;
                     const int32_t cf = cta_of_unit(s.u_pair0, sh.total, C0);
                     const int32_t cl = cta_of_unit(s.u_pair0 + s.n_tiles - 1, sh.total, C0);
                     const int prev = atomicAdd(p.tickets + s.pair, 1);
@@ -648,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 named_bar_sync(1, 128);
                 if (*flag_last) {
                     __threadfence();
-                    const int32_t C0 = gridDim.x;
+                    const int32_t C0 = ncta;
                     const int32_t cf = cta_of_unit(s.u_pair0, sh.total, C0);
                     const int32_t cl = cta_of_unit(s.u_pair0 + s.n_tiles - 1, sh.total, C0);
                     if (active) {

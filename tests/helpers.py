@@ -22,15 +22,21 @@ def to_dev(b, device="cuda"):
     return d
 
 
-def gpu_verify(bd, tile_mode=svp.TILE_AUTO, w=None, out=None, lse=None):
+def gpu_verify(bd, tile_mode=svp.TILE_AUTO, w=None, out=None, lse=None, expect_status=0):
+    """Run the CUDA path with a fresh workspace; check the device status word."""
     kw = {}
     if bd.paged:
         kw = dict(k_cache=bd.k_cache, v_cache=bd.v_cache, block_table=bd.block_table)
     else:
         kw = dict(k_ctx=bd.k_ctx, v_ctx=bd.v_ctx, cu_ctx=bd.cu_ctx)
+    w = w or bd.W
+    ws = svp.Workspace(svp.verify_attn_workspace_size(bd.n, bd.m_cap, w, bd.hq, bd.hkv, bd.d,
+                                                      bd.q.dtype, tile_mode))
     out, lse = svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots,
-                                      w=w or bd.W, tile_mode=tile_mode, out=out, lse=lse, **kw)
+                                      w=w, tile_mode=tile_mode, out=out, lse=lse, ws=ws, **kw)
     torch.cuda.synchronize()
+    st = ws.read_status()
+    assert st == expect_status, f"device status {st:#x}"
     return out, lse
 
 
@@ -59,6 +65,11 @@ def compare_attention(out_gpu, lse_gpu, ref_o, ref_l, rows, dtype):
     """Element-wise comparison on the given packed rows; returns error stats."""
     o = out_gpu.float().cpu().numpy()[rows]
     r = ref_o[rows]
+    bad_g = np.argwhere(~np.isfinite(o))
+    bad_r = np.argwhere(~np.isfinite(r))
+    assert bad_g.size == 0 and bad_r.size == 0, (
+        f"non-finite: gpu {len(bad_g)} (first {bad_g[:4].tolist()}), "
+        f"oracle {len(bad_r)} (first {bad_r[:4].tolist()}), rows {rows[:3].tolist()}...")
     err = np.abs(o.astype(np.float64) - r)
     stats = dict(max_abs=float(err.max()), mean_abs=float(err.mean()),
                  max_rel=float((err / np.maximum(np.abs(r), 1e-3)).max()))

@@ -204,9 +204,20 @@ def test_bad_metadata_sets_status_and_gpu_stays_healthy():
     assert ws.read_status() == 0
 
 
-def test_repeated_calls_are_deterministic():
-    b = wl.make_batch("full_width_bf16", seed=9, n=4, ctx_lengths=[5000, 3000, 8000, 700])
+@pytest.mark.parametrize("ctx", [[5000, 3000, 8000, 700], [10, 70, 0, 3]])
+def test_repeated_calls_are_deterministic_and_leave_tickets_zero(ctx):
+    # the second case has fewer KV tiles than SMs, so some CTAs get no work
+    b = wl.make_batch("full_width_bf16", seed=9, n=4, ctx_lengths=ctx)
     bd = to_dev(b)
-    o1, l1 = gpu_verify(bd)
-    o2, l2 = gpu_verify(bd)
+    ws = svp.Workspace(svp.verify_attn_workspace_size(4, b.m_cap, 16, 32, 8, 128))
+    kw = dict(k_ctx=bd.k_ctx, v_ctx=bd.v_ctx, cu_ctx=bd.cu_ctx, w=16, ws=ws)
+    o1, l1 = svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots, **kw)
+    o2, l2 = svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots, **kw)
+    torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    pairs = 4 * 8   # requests x KV heads (one row block)
+    tickets = ws.buf[256:256 + 4 * pairs].view(torch.int32)
+    assert int(tickets.abs().sum()) == 0
+    assert ws.read_status() == 0
+    ref_o, ref_l = oracle_verify(b)
+    compare_attention(o1, l1, ref_o, ref_l, rows_of(b), torch.bfloat16)
