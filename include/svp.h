@@ -27,9 +27,12 @@
  *     workspace too small, failed launch) are returned synchronously as svp_status and
  *     nothing is enqueued.
  *   - Workspaces: query the size, allocate it once, zero it once with
- *     svp_workspace_init, then reuse it for every later call of the same entry point.
- *     Kernels leave their counters at zero when they finish.  Calls that share one
- *     workspace must not overlap on the GPU.
+ *     svp_workspace_init, then reuse it for later calls of the same entry point.  The
+ *     number of requests, m_cap and w may change from call to call (re-query the size:
+ *     it grows with n); the attention workspace is tied to one head_dim and tile mode
+ *     (a mismatch is reported as SVP_DEV_WORKSPACE and nothing is computed).  Kernels
+ *     leave their counters at zero when they finish.  Calls that share one workspace
+ *     must not overlap on the GPU.  After SVP_DEV_TIMEOUT, zero the workspace again.
  *   - Rows of out/lse that belong to no request (rows >= cu_slots[n], padding) are
  *     never written.
  *   - Kernels never trap.  Every wait inside a kernel is bounded; on expiry the kernel
@@ -59,6 +62,8 @@ typedef enum {
 #define SVP_DEV_BAD_SLOTS   0x1   /* cu_slots decreasing, k_i > w, or cu_slots[n] > m_cap */
 #define SVP_DEV_BAD_CONTEXT 0x2   /* ctx_len < 0 or a context beyond its storage          */
 #define SVP_DEV_TIMEOUT     0x4   /* a bounded in-kernel wait expired                    */
+#define SVP_DEV_WORKSPACE   0x8   /* workspace last used with another head_dim or tile mode:
+                                     nothing was computed; run svp_workspace_init first     */
 
 typedef enum { SVP_F32 = 0, SVP_BF16 = 1 } svp_dtype;
 

@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(_HERE, "libsvp.so")
 SVP_OK, SVP_EINVAL, SVP_EUNSUPPORTED, SVP_EWORKSPACE, SVP_ECUDA = 0, 1, 2, 3, 4
 SVP_F32, SVP_BF16 = 0, 1
 TILE_AUTO, TILE_SHORT, TILE_FIXED128, TILE_WIDE = 0, 1, 2, 3
-DEV_BAD_SLOTS, DEV_BAD_CONTEXT, DEV_TIMEOUT = 0x1, 0x2, 0x4
+DEV_BAD_SLOTS, DEV_BAD_CONTEXT, DEV_TIMEOUT, DEV_WORKSPACE = 0x1, 0x2, 0x4, 0x8
 
 
 class SvpError(RuntimeError):
@@ -256,7 +256,7 @@ def verify_attn_packed(q, k_new, v_new, ctx_len, cu_slots, *, w: int, hkv: Optio
         lse = torch.full((m_cap, hq), float("nan"), dtype=torch.float32, device=q.device)
     nbytes = verify_attn_workspace_size(n, m_cap, w, hq, hkv, d, q.dtype, tile_mode)
     if ws is None:
-        ws = _workspace(("verify", tile_mode, code), nbytes, q.device, stream)
+        ws = _workspace(("verify", tile_mode, code, d), nbytes, q.device, stream)
     h = _heads(hq, hkv, d, scale)
     _check(lib().svp_verify_attn_packed_ex(
         _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), ctypes.byref(kv),
@@ -288,7 +288,7 @@ def prefill_attn(q, k, v, cu_seqlens, *, max_s: int, out=None, lse=None, want_ls
         lse = torch.empty((total_s, hq), dtype=torch.float32, device=q.device)
     nbytes = prefill_attn_workspace_size(n, max_s, hq, hkv, d)
     if ws is None:
-        ws = _workspace(("prefill",), nbytes, q.device, stream)
+        ws = _workspace(("prefill", d), nbytes, q.device, stream)
     h = _heads(hq, hkv, d, scale)
     _check(lib().svp_prefill_attn(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(cu_seqlens, "cu_seqlens", torch.int32),

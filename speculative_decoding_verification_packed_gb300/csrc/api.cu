@@ -12,6 +12,8 @@ namespace svp {
 
 // ---- kernels defined in the other translation units
 svp_status attn_tc_launch(const TcParams &p, int d, int grid, cudaStream_t stream);
+svp_status verify_tc_launch(const TcParams &p, int d, int grid, cudaStream_t stream);
+bool verify_tc_layout(int d, int NR, TcParams &p);
 int attn_tc_max_prefix();
 int attn_tc_block_keys();
 svp_status attn_simt_launch(const SimtParams &p, cudaStream_t stream);
@@ -87,8 +89,8 @@ static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 // ---- tensor-core attention plan (tile router + work split + workspace layout)
 struct AttnPlan {
-    int mode, HP, R, RB, HG, CB, split, grid;
-    size_t off_tickets, off_part_o, off_part_ml, bytes;
+    int mode, HP, R, RB, HG, CB, split, grid, transposed, NR;
+    size_t off_part_ml, off_part_o, off_tickets, bytes;
 };
 
 static svp_status attn_plan(int32_t n, int32_t w, int32_t hq, int32_t hkv, int32_t d,
@@ -105,15 +107,26 @@ static svp_status attn_plan(int32_t n, int32_t w, int32_t hq, int32_t hkv, int32
     pl = AttnPlan{};
     pl.mode = mode;
     switch (mode) {
-    case SVP_TILE_SHORT:
-        if (G > 128)
-            return SVP_EUNSUPPORTED;
-        pl.HP = G;
-        pl.R = std::min(w, 128 / G);
+    case SVP_TILE_SHORT: {
+        // transposed kernel: G*R rows of the tile on the MMA N dimension; TMEM holds two
+        // S^T buffers, O^T (d/128 of them) and l^T, each NR columns wide.
+        const int nr_cap = (d == 256) ? 96 : 128;
+        if (d != 64 && G <= nr_cap) {
+            pl.transposed = 1;
+            pl.HP = G;
+            pl.R = std::min(w, nr_cap / G);
+            pl.NR = (G * pl.R + 31) / 32 * 32;
+        } else {
+            if (G > 128)
+                return SVP_EUNSUPPORTED;
+            pl.HP = G;
+            pl.R = std::min(w, 128 / G);
+        }
         pl.HG = hkv;
         pl.CB = 16;
         pl.split = 1;
         break;
+    }
     case SVP_TILE_FIXED128:
         pl.HP = 1;
         pl.R = std::min(w, 128);
@@ -139,14 +152,16 @@ static svp_status attn_plan(int32_t n, int32_t w, int32_t hq, int32_t hkv, int32
         pl.grid = sm_count();
     else
         pl.grid = (int)std::max<int64_t>(pairs, 1);
+    // header | partial (max, sum) | partial O | tickets: the partial regions depend only
+    // on the device and head_dim, so a workspace can serve calls with different n.
+    const size_t slots = pl.split ? 2 * (size_t)sm_count() : 0;
     size_t o = kWsHeader;
-    pl.off_tickets = o;
-    o = al256(o + sizeof(int32_t) * (size_t)std::max<int64_t>(pairs, 1));
-    pl.off_part_o = o;
-    const size_t slots = pl.split ? 2 * (size_t)pl.grid : 0;
-    o = al256(o + slots * 128 * (size_t)d * sizeof(float));
     pl.off_part_ml = o;
     o = al256(o + slots * 128 * 2 * sizeof(float));
+    pl.off_part_o = o;
+    o = al256(o + slots * 128 * (size_t)d * sizeof(float));
+    pl.off_tickets = o;
+    o = al256(o + sizeof(int32_t) * (size_t)std::max<int64_t>(pairs, 1));
     pl.bytes = o;
     return SVP_OK;
 }
@@ -315,12 +330,12 @@ static svp_status verify_impl(const void *q, const void *k_new, const void *v_ne
             return SVP_EUNSUPPORTED;
     }
     // context
-    const int BK = attn_tc_block_keys();
+    const int BK = pl.transposed ? 128 : attn_tc_block_keys();
     if (kv->paged && kv->num_pages > 0) {
         const uint64_t dims[4] = {(uint64_t)d, 16, (uint64_t)hkv, (uint64_t)kv->num_pages};
         const uint64_t str[3] = {(uint64_t)kv->stride_tok * esz, (uint64_t)kv->stride_head * esz,
                                  (uint64_t)kv->stride_page * esz};
-        const uint32_t box[4] = {64, 16, 1, 1};
+        const uint32_t box[4] = {64, 16, 1, 1};   // one 16-token page of one head
         if (!encode_bf16(&p.tm_kc, kv->k, 4, dims, str, box) ||
             !encode_bf16(&p.tm_vc, kv->v, 4, dims, str, box))
             return SVP_EUNSUPPORTED;
@@ -352,6 +367,12 @@ static svp_status verify_impl(const void *q, const void *k_new, const void *v_ne
     p.tickets = reinterpret_cast<int32_t *>(wsb + pl.off_tickets);
     p.part_o = reinterpret_cast<float *>(wsb + pl.off_part_o);
     p.part_ml = reinterpret_cast<float2 *>(wsb + pl.off_part_ml);
+    p.sig = (pl.transposed << 20) | (pl.mode << 12) | d;
+    if (pl.transposed) {
+        if (!verify_tc_layout(d, pl.NR, p))
+            return SVP_EUNSUPPORTED;
+        return verify_tc_launch(p, d, pl.grid, stream);
+    }
     return attn_tc_launch(p, d, pl.grid, stream);
 }
 

@@ -264,11 +264,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     if (bad_bits && blockIdx.x == 0)
         set_status(p.status, bad_bits);
+    if (tid == 0) {
+        // the workspace layout must match this call's (head_dim, tile mode)
+        const int32_t seen = *reinterpret_cast<volatile int32_t *>(p.status + 1);
+        *flag_last = (seen != 0 && seen != p.sig) ? 1 : 0;
+        if (*flag_last && blockIdx.x == 0)
+            set_status(p.status, SVP_DEV_WORKSPACE);
+        if (seen == 0 && blockIdx.x == 0)
+            p.status[1] = p.sig;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    sh.total = sh.prefix[NQ];
+    const bool ws_bad = *flag_last != 0;
+    sh.total = ws_bad ? 0 : sh.prefix[NQ];
 
     // This CTA's unit range.  The units are cut into ncta = min(grid, units) ranges so
     // that every range is non-empty (a pair's pieces are then consecutive CTAs).
@@ -281,6 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         } else {
             cta_s = cta_e = 0;
         }
+    } else if (ws_bad) {
+        cta_s = cta_e = 0;
     } else {
         // one (request, row block, head group) pair per CTA
         const int32_t pair = blockIdx.x;

@@ -16,8 +16,9 @@
 //     associative (ties: lowest index), so results do not depend on arrival order.
 //   * The CTA that finishes the last chunk of a row (atomic ticket, no waiting)
 //     finalises the row; in the fused kernel the CTA that finalises the last row of a
-//     request then runs the greedy acceptance for that request.  Tickets are reset by
-//     their last user, so a zeroed workspace stays reusable.
+//     request then runs the greedy acceptance for that request.  Tickets, partials and
+//     per-row argmaxes are cleared by their last reader, so the workspace is all zero
+//     again after every call and can serve calls of any size.
 #include <cfloat>
 #include <climits>
 #include <cuda_bf16.h>
@@ -208,6 +209,8 @@ __device__ void finish_request(const MarginArgs &a, int32_t i)
         ++acc;
     a.accept_len[i] = 1 + acc;
     a.next_token[i] = __ldcg(a.row_argmax + off + acc);
+    for (int32_t j = 0; j < k; ++j)      // the workspace returns to zero
+        a.row_argmax[off + j] = 0;
 }
 
 template <bool kBf16>
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kMarginThreads) margin_kernel(MarginArgs a)
         if (s_flag && tid == 0) {
             // last chunk of this row: merge the row's partials in chunk order
             __threadfence();
-            const Top2 *pp = a.partial + row * a.chunks_per_row;
+            Top2 *pp = a.partial + row * a.chunks_per_row;
             Top2 r = top2_identity();
             for (int k = 0; k < a.chunks_per_row; ++k) {
                 Top2 u;
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(kMarginThreads) margin_kernel(MarginArgs a)
                 u.v2 = __ldcg(&pp[k].v2);
                 u.i1 = __ldcg(&pp[k].i1);
                 r = top2_merge(r, u);
+                pp[k] = Top2{0.0f, 0.0f, 0};   // the workspace returns to zero
             }
             a.row_ticket[row] = 0;
             if (a.top1_idx) a.top1_idx[row] = r.i1;

@@ -10,7 +10,7 @@ constexpr int kBN = 64;               // keys per KV tile
 constexpr int kRows = 128;            // query rows per tile (MMA M)
 constexpr int kThreads = 192;         // 6 warps
 constexpr int kSoftmaxWarp0 = 2;
-constexpr int kMaxPrefix = 2048;      // (request, row block) entries held in shared memory
+constexpr int kMaxPrefix = 1024;      // (request, row block) entries held in shared memory
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only when it grows by > 2^8
 
 enum { kModeShort = 1, kModeFixed128 = 2, kModeWide = 3 };
@@ -37,6 +37,10 @@ struct TcParams {
     int32_t *tickets;            // [n * RB * HG]
     float *part_o;               // [2 * gridDim.x][128][d]
     float2 *part_ml;             // [2 * gridDim.x][128]
+    int32_t sig;                 // workspace layout signature (header word 1)
+    // transposed short-tile kernel only: tile rows and shared-memory layout
+    int32_t NR, nslot, tmem_cols, smem_bytes;
+    int32_t off_q, off_p, off_ones, off_ring, off_bar, off_misc, off_pref;
 };
 
 struct SimtParams {

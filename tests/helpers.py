@@ -9,6 +9,9 @@ import speculative_decoding_verification_packed_gb300 as svp
 BF16_MAX_ABS = 2e-2     # attention bars for bf16 inputs with fp32 accumulation
 BF16_MEAN_ABS = 2e-3
 F32_MAX_ABS = 1e-4      # attention bar for fp32 inputs
+# lse for bf16 inputs: the row sum l is accumulated from P rounded to bf16 (the same
+# weights O uses), so |d l / l| <= 2^-9 and |d lse| <= ln(1 + 2^-9) ~ 1.95e-3; bar 2x that.
+BF16_LSE_ABS = 4e-3
 
 
 def to_dev(b, device="cuda"):
@@ -84,6 +87,6 @@ def compare_attention(out_gpu, lse_gpu, ref_o, ref_l, rows, dtype):
         assert stats["max_abs"] <= BF16_MAX_ABS, stats
         assert stats["mean_abs"] <= BF16_MEAN_ABS, stats
         if lse_gpu is not None:
-            assert stats["lse_max_abs"] <= 1e-3, stats
+            assert stats["lse_max_abs"] <= BF16_LSE_ABS, stats
     assert np.isfinite(o).all()
     return stats

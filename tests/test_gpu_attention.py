@@ -2,8 +2,8 @@
 
 Same seeded inputs on both sides; element-wise comparison on every packed row (small
 and medium cases) or on sampled requests (full-size paged and wide-head workloads).
-Bars: bf16 max-abs 2e-2 and mean-abs 2e-3, fp32 max-abs 1e-4; lse within 1e-3 (bf16)
-or 1e-4 (fp32).
+Bars: bf16 max-abs 2e-2 and mean-abs 2e-3, fp32 max-abs 1e-4; lse within 4e-3 (bf16:
+twice the bf16 rounding bound of the row sum) or 1e-4 (fp32).
 """
 import numpy as np
 import pytest
@@ -215,9 +215,33 @@ def test_repeated_calls_are_deterministic_and_leave_tickets_zero(ctx):
     o2, l2 = svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots, **kw)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    pairs = 4 * 8   # requests x KV heads (one row block)
-    tickets = ws.buf[256:256 + 4 * pairs].view(torch.int32)
+    pairs = 4 * 8   # requests x KV heads (one row block): tickets are the last words
+    tickets = ws.buf[-1024:].view(torch.int32)
     assert int(tickets.abs().sum()) == 0
     assert ws.read_status() == 0
     ref_o, ref_l = oracle_verify(b)
     compare_attention(o1, l1, ref_o, ref_l, rows_of(b), torch.bfloat16)
+
+
+def test_workspace_reuse_across_sizes_and_mismatch_flag():
+    # one workspace serves calls with different n; a different head_dim is refused
+    big = wl.make_batch("budget8n_bf16", seed=11, n=6, lengths=[16, 3, 9, 1, 12, 7],
+                        ctx_lengths=[900, 20, 3000, 5, 130, 64], hq=8, hkv=2, d=128)
+    small = wl.make_batch("budget8n_bf16", seed=12, n=2, lengths=[5, 16],
+                          ctx_lengths=[70, 400], hq=8, hkv=2, d=128)
+    ws = svp.Workspace(max(svp.verify_attn_workspace_size(6, big.m_cap, 16, 8, 2, 128),
+                           svp.verify_attn_workspace_size(6, big.m_cap, 16, 8, 2, 256)))
+    for b in (small, big, small):
+        bd = to_dev(b)
+        o, l = svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots, w=16,
+                                      ws=ws, k_ctx=bd.k_ctx, v_ctx=bd.v_ctx, cu_ctx=bd.cu_ctx)
+        torch.cuda.synchronize()
+        assert ws.read_status() == 0
+        ref_o, ref_l = oracle_verify(b)
+        compare_attention(o, l, ref_o, ref_l, rows_of(b), torch.bfloat16)
+    other = wl.make_batch("budget8n_bf16", seed=13, n=2, lengths=[5, 16],
+                          ctx_lengths=[70, 400], hq=8, hkv=2, d=256)
+    bd = to_dev(other)
+    svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots, w=16, ws=ws,
+                           k_ctx=bd.k_ctx, v_ctx=bd.v_ctx, cu_ctx=bd.cu_ctx)
+    assert ws.read_status() & svp.DEV_WORKSPACE

@@ -147,3 +147,25 @@ def test_repeated_margin_calls_reuse_workspace():
     torch.cuda.synchronize()
     for u, v in zip(a, b):
         assert torch.equal(u, v)
+
+
+def test_margin_workspace_returns_to_zero_and_serves_any_size():
+    ws = svp.Workspace(svp.margin_accept_workspace_size(40, 300, 5000))
+    g = torch.Generator().manual_seed(9)
+    for m_cap, n in ((300, 40), (20, 3), (300, 40)):
+        lengths = torch.randint(0, 8, (n,), generator=g)
+        cu = torch.zeros(n + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(lengths, 0)
+        cu = cu.clamp(max=m_cap)
+        logits = torch.randn(m_cap, 5000, generator=g)
+        tokens = torch.randint(0, 5000, (m_cap,), generator=g, dtype=torch.int32)
+        outs = svp.margin_accept(logits.cuda(), tokens.cuda(), cu.cuda(), ws=ws)
+        torch.cuda.synchronize()
+        live = int(cu[-1])
+        r_idx = _check_rows(logits[:live], [o[:live] for o in outs[:4]])
+        acc, nxt = oracle.greedy_accept(np.concatenate([r_idx, np.zeros(m_cap - live, np.int32)]),
+                                        tokens, cu)
+        assert np.array_equal(outs[4].cpu().numpy(), acc)
+        assert np.array_equal(outs[5].cpu().numpy(), nxt)
+        assert ws.read_status() == 0
+        assert int(ws.buf[256:].to(torch.int32).sum()) == 0
