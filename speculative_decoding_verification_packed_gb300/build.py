@@ -20,6 +20,8 @@ LIB = os.path.join(HERE, "libsvp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
+# optional extra nvcc flags (e.g. -DSVP_WAIT_SLEEP_NS=200 for tuning runs)
+FLAGS += os.environ.get("SVP_NVCC_FLAGS", "").split()
 
 
 def nvcc() -> str:

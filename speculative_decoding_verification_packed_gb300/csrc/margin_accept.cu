@@ -7,15 +7,15 @@
 // supplies the successor).
 //
 // Design (HBM-bound stream, no tensor cores):
-//   * Each logits row is cut into equal chunks of <= 16384 elements; a persistent grid
-//     (a multiple of the SM count) strides over all (row, chunk) pairs.
-//   * Each thread keeps a (top1, top1_idx, top2) triple over 16-byte vector loads that
-//     are all issued before use; a vector whose maximum cannot beat the current top-2
-//     is skipped after one packed max.
-//   * Triples merge by warp shuffles and shared memory; the merge is commutative and
-//     associative (ties: lowest index), so results do not depend on arrival order.
-//   * The CTA that finishes the last chunk of a row (atomic ticket, no waiting)
-//     finalises the row; in the fused kernel the CTA that finalises the last row of a
+//   * Each logits row is cut into equal chunks of <= 8192 elements; every warp is an
+//     independent worker on one (row, chunk) unit at a time (no CTA barriers).
+//   * Each lane keeps a (top1, top1_idx, top2) triple over 16-byte vector loads, eight
+//     in flight at once; a vector whose maximum cannot beat the current top-2 is
+//     skipped after one packed max.
+//   * Triples merge by warp shuffles; the merge is commutative and associative (ties:
+//     lowest index), so results do not depend on arrival order.
+//   * The warp that finishes the last chunk of a row (atomic ticket, no waiting)
+//     finalises the row; in the fused kernel the warp that finalises the last row of a
 //     request then runs the greedy acceptance for that request.  Tickets, partials and
 //     per-row argmaxes are cleared by their last reader, so the workspace is all zero
 //     again after every call and can serve calls of any size.
@@ -107,15 +107,16 @@ struct MarginArgs {
     int32_t *next_token;
 };
 
-constexpr int kMarginThreads = 256;
-constexpr int kMarginUnroll = 8;
+constexpr int kMarginThreads = 256;      // 8 independent warps per CTA
+constexpr int kMarginBatch = 8;          // 16-byte loads in flight per lane
+
 
 // Which request owns packed row r (cu_slots non-decreasing, validated by the caller).
 __device__ __forceinline__ int32_t owner_of_row(const int32_t *cu, int32_t n, int32_t r)
 {
-    int32_t lo = 0, hi = n;   // find the largest i with cu[i] <= r, among i < n
+    int32_t lo = 0, hi = n;   // the largest i < n with cu[i] <= r
     while (hi - lo > 1) {
-        int32_t mid = (lo + hi) >> 1;
+        const int32_t mid = (lo + hi) >> 1;
         if (__ldg(cu + mid) <= r)
             lo = mid;
         else
@@ -125,29 +126,35 @@ __device__ __forceinline__ int32_t owner_of_row(const int32_t *cu, int32_t n, in
 }
 
 template <bool kBf16>
-__device__ __forceinline__ Top2 scan_chunk(const MarginArgs &a, int64_t row, int32_t c0, int32_t c1)
+__device__ __forceinline__ float load_elem(const MarginArgs &a, int64_t row, int32_t e)
+{
+    if (kBf16)
+        return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(a.logits)[row * a.row_stride + e] << 16);
+    return reinterpret_cast<const float *>(a.logits)[row * a.row_stride + e];
+}
+
+// One warp scans elements [c0, c1) of a row; lane-local triples, indices increasing.
+template <bool kBf16>
+__device__ __forceinline__ Top2 scan_chunk_warp(const MarginArgs &a, int64_t row, int32_t c0,
+                                                int32_t c1, int lane)
 {
     Top2 t = top2_identity();
-    const int tid = threadIdx.x;
     constexpr int VW = kBf16 ? 8 : 4;        // elements per 16-byte vector
+    int32_t done = c0;
     if (a.vec_ok) {
         const int32_t nvec = (c1 - c0) / VW;
-        const uint8_t *base = reinterpret_cast<const uint8_t *>(a.logits) +
-                              (row * a.row_stride + c0) * (kBf16 ? 2 : 4);
-        const uint4 *vp = reinterpret_cast<const uint4 *>(base);
-        for (int32_t v0 = 0; v0 < nvec; v0 += kMarginThreads * kMarginUnroll) {
-            uint4 buf[kMarginUnroll];
+        const uint4 *vp = reinterpret_cast<const uint4 *>(
+            reinterpret_cast<const uint8_t *>(a.logits) + (row * a.row_stride + c0) * (kBf16 ? 2 : 4));
+        for (int32_t v0 = 0; v0 < nvec; v0 += 32 * kMarginBatch) {
+            uint4 buf[kMarginBatch];
 #pragma unroll
-            for (int u = 0; u < kMarginUnroll; ++u) {
-                const int32_t v = v0 + u * kMarginThreads + tid;
-                if (v < nvec)
-                    buf[u] = __ldcs(vp + v);
-                else
-                    buf[u] = make_uint4(0, 0, 0, 0);
+            for (int u = 0; u < kMarginBatch; ++u) {
+                const int32_t v = v0 + u * 32 + lane;
+                buf[u] = (v < nvec) ? __ldcs(vp + v) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < kMarginUnroll; ++u) {
-                const int32_t v = v0 + u * kMarginThreads + tid;
+            for (int u = 0; u < kMarginBatch; ++u) {
+                const int32_t v = v0 + u * 32 + lane;
                 if (v >= nvec)
                     break;
                 const int32_t e0 = c0 + v * VW;
@@ -178,25 +185,10 @@ __device__ __forceinline__ Top2 scan_chunk(const MarginArgs &a, int64_t row, int
                 }
             }
         }
-        // ragged tail of the chunk (only the row's last chunk can have one)
-        for (int32_t e = c0 + nvec * VW + tid; e < c1; e += kMarginThreads) {
-            float x;
-            if (kBf16)
-                x = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(a.logits)[row * a.row_stride + e] << 16);
-            else
-                x = reinterpret_cast<const float *>(a.logits)[row * a.row_stride + e];
-            top2_push(t, x, e);
-        }
-    } else {
-        for (int32_t e = c0 + tid; e < c1; e += kMarginThreads) {
-            float x;
-            if (kBf16)
-                x = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(a.logits)[row * a.row_stride + e] << 16);
-            else
-                x = reinterpret_cast<const float *>(a.logits)[row * a.row_stride + e];
-            top2_push(t, x, e);
-        }
+        done = c0 + nvec * VW;
     }
+    for (int32_t e = done + lane; e < c1; e += 32)      // ragged tail / unaligned rows
+        top2_push(t, load_elem<kBf16>(a, row, e), e);
     return t;
 }
 
@@ -216,69 +208,57 @@ __device__ void finish_request(const MarginArgs &a, int32_t i)
 template <bool kBf16>
 __global__ void __launch_bounds__(kMarginThreads) margin_kernel(MarginArgs a)
 {
-    __shared__ Top2 warp_part[kMarginThreads / 32];
-    __shared__ int s_flag;
-    __shared__ int32_t s_live_rows;
-    __shared__ int s_valid;
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarp = ((int64_t)blockIdx.x * kMarginThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kMarginThreads) >> 5;
 
-    // Fused mode: validate cu_slots once per CTA; rows >= cu[n] are not read.
-    if (tid == 0) {
-        int32_t live = a.rows;
-        int valid = 1;
-        if (a.cu_slots) {
-            int bad = (__ldg(a.cu_slots) != 0);
-            for (int32_t i = 0; i < a.n && !bad; ++i)
-                bad = __ldg(a.cu_slots + i + 1) < __ldg(a.cu_slots + i);
-            live = __ldg(a.cu_slots + a.n);
-            if (bad || live > a.rows || live < 0) {
-                live = 0;
-                valid = 0;
-                if (blockIdx.x == 0)
-                    set_status(a.status, SVP_DEV_BAD_SLOTS);
-            }
+    // fused mode: rows >= cu[n] are not read; invalid cu_slots -> nothing is read
+    int32_t live_rows = a.rows;
+    bool valid = true;
+    if (a.cu_slots) {
+        bool bad = (lane == 0) && (__ldg(a.cu_slots) != 0);
+        for (int32_t i = lane; i < a.n; i += 32)
+            bad |= __ldg(a.cu_slots + i + 1) < __ldg(a.cu_slots + i);
+        live_rows = __ldg(a.cu_slots + a.n);
+        bad |= live_rows > a.rows || live_rows < 0;
+        valid = !__any_sync(0xffffffffu, bad);
+        if (!valid) {
+            live_rows = 0;
+            if (gwarp == 0 && lane == 0)
+                set_status(a.status, SVP_DEV_BAD_SLOTS);
         }
-        s_live_rows = live;
-        s_valid = valid;
     }
-    __syncthreads();
-    const int32_t live_rows = s_live_rows;
-    const int64_t total = (int64_t)live_rows * a.chunks_per_row;
+    const int64_t units = (int64_t)live_rows * a.chunks_per_row;
 
-    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+    for (int64_t w = gwarp; w < units; w += nwarps) {
         const int64_t row = w / a.chunks_per_row;
         const int32_t ch = (int32_t)(w % a.chunks_per_row);
         const int32_t c0 = ch * a.chunk;
         const int32_t c1 = min(a.vocab, c0 + a.chunk);
-        Top2 t = scan_chunk<kBf16>(a, row, c0, c1);
-        t = top2_warp_merge(t);
-        if (lane == 0)
-            warp_part[warp] = t;
-        __syncthreads();
-        if (tid == 0) {
-            Top2 r = warp_part[0];
-            for (int k = 1; k < kMarginThreads / 32; ++k)
-                r = top2_merge(r, warp_part[k]);
-            a.partial[row * a.chunks_per_row + ch] = r;
+        Top2 t = top2_warp_merge(scan_chunk_warp<kBf16>(a, row, c0, c1, lane));
+        int last = 0;
+        if (lane == 0) {
+            a.partial[row * a.chunks_per_row + ch] = t;
             __threadfence();
-            const int prev = atomicAdd(a.row_ticket + row, 1);
-            s_flag = (prev == a.chunks_per_row - 1);
+            last = atomicAdd(a.row_ticket + row, 1) == a.chunks_per_row - 1;
         }
-        __syncthreads();
-        if (s_flag && tid == 0) {
-            // last chunk of this row: merge the row's partials in chunk order
-            __threadfence();
-            Top2 *pp = a.partial + row * a.chunks_per_row;
-            Top2 r = top2_identity();
-            for (int k = 0; k < a.chunks_per_row; ++k) {
-                Top2 u;
-                u.v1 = __ldcg(&pp[k].v1);
-                u.v2 = __ldcg(&pp[k].v2);
-                u.i1 = __ldcg(&pp[k].i1);
-                r = top2_merge(r, u);
-                pp[k] = Top2{0.0f, 0.0f, 0};   // the workspace returns to zero
-            }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last)
+            continue;
+        // last chunk of this row: merge its partials (lane-parallel) and clear them
+        __threadfence();
+        Top2 *pp = a.partial + row * a.chunks_per_row;
+        Top2 r = top2_identity();
+        for (int32_t k = lane; k < a.chunks_per_row; k += 32) {
+            Top2 u;
+            u.v1 = __ldcg(&pp[k].v1);
+            u.v2 = __ldcg(&pp[k].v2);
+            u.i1 = __ldcg(&pp[k].i1);
+            r = top2_merge(r, u);
+            pp[k] = Top2{0.0f, 0.0f, 0};
+        }
+        r = top2_warp_merge(r);
+        if (lane == 0) {
             a.row_ticket[row] = 0;
             if (a.top1_idx) a.top1_idx[row] = r.i1;
             if (a.top1) a.top1[row] = r.v1;
@@ -289,20 +269,18 @@ __global__ void __launch_bounds__(kMarginThreads) margin_kernel(MarginArgs a)
                 __threadfence();
                 const int32_t i = owner_of_row(a.cu_slots, a.n, (int32_t)row);
                 const int32_t k = __ldg(a.cu_slots + i + 1) - __ldg(a.cu_slots + i);
-                const int prev = atomicAdd(a.req_ticket + i, 1);
-                if (prev == k - 1) {
+                if (atomicAdd(a.req_ticket + i, 1) == k - 1) {
                     __threadfence();
                     a.req_ticket[i] = 0;
                     finish_request(a, i);
                 }
             }
         }
-        __syncthreads();
     }
 
-    // Inactive requests (k_i = 0) have no rows: block 0 writes their results.
-    if (a.cu_slots && blockIdx.x == 0 && s_valid) {
-        for (int32_t i = tid; i < a.n; i += kMarginThreads) {
+    // inactive requests (k_i = 0) have no rows: the first warp writes their results
+    if (a.cu_slots && gwarp == 0 && valid) {
+        for (int32_t i = lane; i < a.n; i += 32) {
             if (__ldg(a.cu_slots + i + 1) == __ldg(a.cu_slots + i)) {
                 a.accept_len[i] = 0;
                 a.next_token[i] = -1;
@@ -348,7 +326,7 @@ struct MarginPlan {
 static MarginPlan margin_plan(int32_t rows, int32_t vocab, int32_t n)
 {
     MarginPlan p{};
-    const int32_t target = 16384;
+    const int32_t target = 8192;   // elements per unit (16 KB of bf16), one warp each
     p.chunks_per_row = (vocab + target - 1) / target;
     if (p.chunks_per_row < 1)
         p.chunks_per_row = 1;
@@ -421,10 +399,11 @@ svp_status margin_launch(const void *logits, int64_t row_stride, int32_t rows, i
     a.n = n;
     a.accept_len = accept_len;
     a.next_token = next_token;
+    // one unit per warp, capped at eight resident CTAs of 8 warps per SM (grid-stride)
     const int64_t work = (int64_t)rows * p.chunks_per_row;
-    int64_t grid = (int64_t)sm_count() * 4;
-    if (grid > work)
-        grid = work;
+    int64_t grid = (work + kMarginThreads / 32 - 1) / (kMarginThreads / 32);
+    if (grid > (int64_t)sm_count() * 8)
+        grid = (int64_t)sm_count() * 8;
     if (grid < 1)
         grid = 1;
     if (dtype == SVP_BF16)

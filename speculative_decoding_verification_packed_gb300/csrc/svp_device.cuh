@@ -61,6 +61,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds for the phase.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Longest sleep (ns) a waiting thread asks for between polls of an mbarrier.
+#ifndef SVP_WAIT_SLEEP_NS
+#define SVP_WAIT_SLEEP_NS 0
+#endif
+
 // Bounded wait for the phase with the given parity to complete.  Returns false when
 // `abort_flag` (shared memory) is raised by another role or when the time limit
 // expires; in the latter case the caller raises the flag itself.
@@ -73,9 +92,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
         return true;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+        if (SVP_WAIT_SLEEP_NS > 0 ? mbar_try_wait_sleep(bar, parity, SVP_WAIT_SLEEP_NS)
+                                  : mbar_try_wait(bar, parity))
             return true;
-        if ((it & 63u) == 0) {
+        if ((it & 15u) == 0) {
             if (*abort_flag)
                 return false;
             if (global_ns() - t0 > kWaitLimitNs) {
@@ -253,6 +273,24 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ int4 ld_shared_i4(uint32_t addr)
+{
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)

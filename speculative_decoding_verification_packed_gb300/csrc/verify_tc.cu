@@ -14,11 +14,12 @@
 //   O^T += V^T P^T   M=128 d,    N=rows, K=keys         (TMEM, one per 128 columns of d)
 //   l^T += 1 P^T     M=128,      N=rows, K=keys         (row sums on the tensor core)
 // Every softmax thread owns one key and touches only the live rows.  The running
-// maximum of each row is a stale reference m_ref: P = 2^(s*c - m_ref) is used while
-// no visible score exceeds m_ref + 8; only then (and on the first tile of a piece) the
-// softmax warps reduce the row maxima across keys, move m_ref, and rescale O^T and l^T
-// in TMEM.  Inactive rows carry m_ref = +inf, so their P is 0 without per-element
-// masks.
+// maximum of each row is a stale reference m_ref, seeded on the first tile of a piece
+// with the score of its first key: P = 2^(s*c - m_ref) is used while no visible score
+// exceeds m_ref + 32 (bf16 P and the fp32 accumulators hold 2^32 exactly in relative
+// terms); only then the softmax warps reduce the row maxima across keys, move m_ref,
+// and rescale O^T and l^T in TMEM.  Inactive rows carry m_ref = +inf, so their P is 0
+// without per-element masks.
 //
 // Pipeline: warp 0 issues TMA into a ring of 32 KB slots ([128 keys][128 d] halves of
 // K, then of V), warp 1 owns TMEM and issues tcgen05.mma from one thread, warps 2..5
@@ -36,7 +37,7 @@ constexpr int kVK = 128;            // keys per KV tile
 constexpr int kVThreads = 192;
 constexpr int kSlotBytes = 32768;   // [128 keys][128 d] bf16 = 2 x [128][64] SW128
 constexpr int kSubBytes = 16384;    // [128 keys][64 d]
-constexpr float kSlack = 8.0f;      // P <= 2^8
+constexpr float kSlack = 32.0f;     // P <= 2^32 (exact in bf16 / fp32 accumulation)
 
 // Shared per-row softmax state (in the misc region).
 struct VtRows {
@@ -45,6 +46,9 @@ struct VtRows {
     float red[4][128];
     int32_t jr[128];     // candidate index of the row (INT_MAX for padding rows)
     float lrow[128];
+    float wts[8][128];   // combine: per-piece weight of each row
+    int64_t orow[128];   // epilogue: output element offset of row r (-1: not a live row)
+    float linv[128];     // epilogue: 1 / l of row r
     int32_t flag[2];
     int32_t rescale;
     int32_t last;
@@ -165,6 +169,53 @@ __device__ __forceinline__ float warp_transpose_max32(float (&v)[32], int lane)
     return v[0];
 }
 
+// P for one 32-row chunk of this thread's key: y = s*c - m_ref, P = 2^y (0 where the
+// key is not visible).  ymax collects the largest visible y (the hit test).
+// cand: candidate tile, key index ckey must be <= the row's candidate index.
+__device__ __forceinline__ void vt_chunk(const uint32_t (&sr)[32], uint32_t mref_addr,
+                                         uint32_t jr_addr, bool key_ok, bool cand, int ckey,
+                                         float cl2, uint32_t *pk, float &ymax)
+{
+    float y[32];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        const float4 m = ld_shared_f4(mref_addr + 16 * v);
+        y[4 * v + 0] = fmaf(__uint_as_float(sr[4 * v + 0]), cl2, -m.x);
+        y[4 * v + 1] = fmaf(__uint_as_float(sr[4 * v + 1]), cl2, -m.y);
+        y[4 * v + 2] = fmaf(__uint_as_float(sr[4 * v + 2]), cl2, -m.z);
+        y[4 * v + 3] = fmaf(__uint_as_float(sr[4 * v + 3]), cl2, -m.w);
+    }
+    if (cand) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const int4 j = ld_shared_i4(jr_addr + 16 * v);
+            if (ckey > j.x) y[4 * v + 0] = -INFINITY;
+            if (ckey > j.y) y[4 * v + 1] = -INFINITY;
+            if (ckey > j.z) y[4 * v + 2] = -INFINITY;
+            if (ckey > j.w) y[4 * v + 3] = -INFINITY;
+        }
+    }
+    if (!key_ok) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            pk[e] = 0u;
+        return;
+    }
+    float t16[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        t16[e] = fmaxf(y[2 * e], y[2 * e + 1]);
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e)
+            t16[e] = fmaxf(t16[e], t16[e + w]);
+    ymax = fmaxf(ymax, t16[0]);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        pk[e] = pack_bf16x2(fast_exp2(y[2 * e]), fast_exp2(y[2 * e + 1]));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_constant__ TcParams p)
 {
@@ -192,6 +243,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
     volatile int *abort_flag = &rs->abort_flag;
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + p.off_pref);
     const int32_t NQ = p.n * p.RB;
+    // start the workspace-signature load early; it is checked after the prologue
+    const int32_t sig_seen = (tid == 0) ? *reinterpret_cast<volatile int32_t *>(p.status + 1) : 0;
 
     if (tid == 0) {
         for (int s = 0; s < nslot; ++s) {
@@ -269,7 +322,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         set_status(p.status, bad_bits);
     if (tid == 0) {
         // the workspace layout must match this call's (head_dim, tile mode)
-        const int32_t seen = *reinterpret_cast<volatile int32_t *>(p.status + 1);
+        const int32_t seen = sig_seen;
         rs->last = (seen != 0 && seen != p.sig) ? 1 : 0;
         if (rs->last && blockIdx.x == 0)
             set_status(p.status, SVP_DEV_WORKSPACE);
@@ -291,67 +344,80 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
 
     if (warp == 0) {
         // ================================================================ producer
-        if (lane == 0) {
-            uint32_t it = 0, nseg = 0, seq = 0;
-            bool ok = true;
-            for (int64_t u = cta_s; u < cta_e && ok;) {
-                VtSeg s;
-                vt_seg(p, prefix, NQ, u, cta_e, cta_s, s);
-                const int32_t off = __ldg(p.cu_slots + s.i);
-                const int32_t L = p.ctx_len ? __ldg(p.ctx_len + s.i) : 0;
-                const int32_t g = (s.hg * p.HP) / p.G;
-                if (nseg > 0 && !(ok = mbar_wait(bar_qempty, (nseg - 1) & 1, abort_flag)))
+        // The whole warp runs the loop; lane 0 issues TMA.  For paged context the lanes
+        // fetch a tile's page ids in parallel (shared by its K and V), one tile ahead.
+        uint32_t it = 0, nseg = 0, seq = 0;
+        bool ok = true;
+        for (int64_t u = cta_s; u < cta_e && ok;) {
+            VtSeg s;
+            vt_seg(p, prefix, NQ, u, cta_e, cta_s, s);
+            const int32_t off = __ldg(p.cu_slots + s.i);
+            const int32_t L = p.ctx_len ? __ldg(p.ctx_len + s.i) : 0;
+            const int32_t g = (s.hg * p.HP) / p.G;
+            const int32_t npages = (L + 15) / 16;
+            const int32_t *bt_row = p.paged ? p.block_table + (int64_t)s.i * p.max_pages : nullptr;
+            if (nseg > 0) {
+                // lane 0 waits, the warp follows (keeps `ok` warp-uniform)
+                int w_ok = 1;
+                if (lane == 0)
+                    w_ok = mbar_wait(bar_qempty, (nseg - 1) & 1, abort_flag);
+                if (!(ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0))
                     break;
+            }
+            if (lane == 0) {
                 mbar_arrive_expect_tx(bar_qfull, (uint32_t)((D / 64) * 64 * p.HP * p.R * 2));
                 for (int dc = 0; dc < D / 64; ++dc)
                     tma_load_3d(sbase + p.off_q + dc * QSUB, &p.tm_q, bar_qfull, dc * 64,
                                 s.hg * p.HP, off + s.rb * p.R);
-                ++nseg;
-                const int64_t cctx = (!p.paged && L > 0) ? __ldg(p.cu_ctx + s.i) : 0;
-                for (int32_t t = s.t0; t < s.t1 && ok; ++t, ++it) {
-                    // K halves then V halves of this tile, one ring slot each
-                    for (int kv = 0; kv < 2 && ok; ++kv) {
-                        const CUtensorMap *mc = kv ? &p.tm_vc : &p.tm_kc;
-                        const CUtensorMap *mn = kv ? &p.tm_vn : &p.tm_kn;
-                        for (int h = 0; h < DH; ++h, ++seq) {
-                            const int sl = seq % nslot;
-                            if (!(ok = mbar_wait(bar_empty(sl), ((seq / nslot) & 1) ^ 1, abort_flag)))
-                                break;
-                            const uint32_t dst = sbase + p.off_ring + sl * kSlotBytes;
+            }
+            ++nseg;
+            const int64_t cctx = (!p.paged && L > 0) ? __ldg(p.cu_ctx + s.i) : 0;
+            // page id of lane pp (< 8) for context tile t
+            auto page_id = [&](int32_t t) -> int32_t {
+                const int32_t pg = t * (kVK / 16) + lane;
+                if (!p.paged || lane >= kVK / 16 || t >= s.n_ctx || pg >= npages)
+                    return -1;
+                return __ldg(bt_row + pg);
+            };
+            int32_t id_next = page_id(s.t0);
+            for (int32_t t = s.t0; t < s.t1 && ok; ++t, ++it) {
+                int32_t id = id_next;
+                id_next = page_id(t + 1);                // prefetch the next tile's ids
+                if (id >= p.num_pages || (id < 0 && p.paged && t < s.n_ctx &&
+                                          lane < kVK / 16 && t * (kVK / 16) + lane < npages)) {
+                    set_status(p.status, SVP_DEV_BAD_CONTEXT);
+                    id = -1;
+                }
+                const uint32_t vmask = __ballot_sync(0xffffffffu, id >= 0);
+                const int32_t nv = __popc(vmask);
+                // K halves then V halves of this tile, one ring slot each
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const CUtensorMap *mc = kv ? &p.tm_vc : &p.tm_kc;
+                    const CUtensorMap *mn = kv ? &p.tm_vn : &p.tm_kn;
+                    for (int h = 0; h < DH; ++h, ++seq) {
+                        const int sl = seq % nslot;
+                        int w_ok = 1;
+                        if (lane == 0)
+                            w_ok = mbar_wait(bar_empty(sl), ((seq / nslot) & 1) ^ 1, abort_flag);
+                        if (!(ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0))
+                            break;
+                        const uint32_t dst = sbase + p.off_ring + sl * kSlotBytes;
+                        if (t < s.n_ctx && p.paged) {
+                            if (lane == 0)
+                                mbar_arrive_expect_tx(bar_full(sl), (uint32_t)(nv * 2 * 2048));
+                            __syncwarp();
+                            if (id >= 0) {      // lane pp issues page pp
+                                for (int c = 0; c < 2; ++c)
+                                    tma_load_4d(dst + c * kSubBytes + lane * 2048, mc, bar_full(sl),
+                                                h * 128 + c * 64, 0, g, id);
+                            }
+                        } else if (lane == 0) {
                             if (t < s.n_ctx) {
-                                if (!p.paged) {
-                                    mbar_arrive_expect_tx(bar_full(sl), (uint32_t)kSlotBytes);
-                                    const int32_t row = (int32_t)(cctx + (int64_t)t * kVK);
-                                    for (int c = 0; c < 2; ++c)
-                                        tma_load_3d(dst + c * kSubBytes, mc, bar_full(sl),
-                                                    h * 128 + c * 64, g, row);
-                                } else {
-                                    const int32_t pg0 = t * (kVK / 16);
-                                    const int32_t npg = min(kVK / 16, (L + 15) / 16 - pg0);
-                                    int32_t ids[kVK / 16];
-                                    int32_t nv = 0;
-                                    for (int pp = 0; pp < kVK / 16; ++pp) {
-                                        ids[pp] = -1;
-                                        if (pp < npg) {
-                                            const int32_t id = __ldg(p.block_table +
-                                                                     (int64_t)s.i * p.max_pages + pg0 + pp);
-                                            if (id >= 0 && id < p.num_pages) {
-                                                ids[pp] = id;
-                                                ++nv;
-                                            } else {
-                                                set_status(p.status, SVP_DEV_BAD_CONTEXT);
-                                            }
-                                        }
-                                    }
-                                    mbar_arrive_expect_tx(bar_full(sl), (uint32_t)(nv * 2 * 2048));
-                                    for (int pp = 0; pp < kVK / 16; ++pp) {
-                                        if (ids[pp] < 0)
-                                            continue;
-                                        for (int c = 0; c < 2; ++c)
-                                            tma_load_4d(dst + c * kSubBytes + pp * 2048, mc,
-                                                        bar_full(sl), h * 128 + c * 64, 0, g, ids[pp]);
-                                    }
-                                }
+                                mbar_arrive_expect_tx(bar_full(sl), (uint32_t)kSlotBytes);
+                                const int32_t row = (int32_t)(cctx + (int64_t)t * kVK);
+                                for (int c = 0; c < 2; ++c)
+                                    tma_load_3d(dst + c * kSubBytes, mc, bar_full(sl),
+                                                h * 128 + c * 64, g, row);
                             } else {
                                 const int32_t ct = t - s.n_ctx;
                                 mbar_arrive_expect_tx(bar_full(sl), (uint32_t)(2 * p.CB * 128));
@@ -360,18 +426,19 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                                                 h * 128 + c * 64, g, off + ct * p.CB);
                             }
                         }
+                        __syncwarp();
                     }
                 }
-                u += (s.t1 - s.t0);
             }
-            if (!ok) {
-                volatile int drain_abort = 0;
-                const uint32_t first = seq > (uint32_t)nslot ? seq - nslot : 0;
-                for (uint32_t k = first; k < seq; ++k)
-                    mbar_wait(bar_full(k % nslot), (k / nslot) & 1, &drain_abort);
-                if (nseg > 0)
-                    mbar_wait(bar_qfull, (nseg - 1) & 1, &drain_abort);
-            }
+            u += (s.t1 - s.t0);
+        }
+        if (!ok && lane == 0) {
+            volatile int drain_abort = 0;
+            const uint32_t first = seq > (uint32_t)nslot ? seq - nslot : 0;
+            for (uint32_t k = first; k < seq; ++k)
+                mbar_wait(bar_full(k % nslot), (k / nslot) & 1, &drain_abort);
+            if (nseg > 0)
+                mbar_wait(bar_qfull, (nseg - 1) & 1, &drain_abort);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
@@ -500,35 +567,58 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 if (!(ok = mbar_wait(bar_sfull(b), (it >> 1) & 1, abort_flag)))
                     break;
                 tc_fence_after();
+                const uint32_t sa = tmem + lane_off + TM_S + b * NR;
+                const uint32_t pline = sbase + p.off_p + t * 128;
+                const uint32_t mref_a = smem_u32(rs->m_ref), jr_a = smem_u32(rs->jr);
+                if (k == 0) {
+                    // seed the reference of every live row with the score of key 0 of
+                    // this piece's first tile (lane 0 of the first lane quarter)
+                    if (quarter == 0) {
+                        for (int c = 0; c < nch; ++c) {
+                            uint32_t sr[32];
+                            tmem_ld32(sa + c * 32, sr);
+                            tmem_wait_ld();
+                            // lane e takes key 0's score of row 32c + e
+                            float mine = 0.0f;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const float v = __shfl_sync(0xffffffffu, __uint_as_float(sr[e]), 0);
+                                if (lane == e)
+                                    mine = v;
+                            }
+                            const int r = c * 32 + lane;
+                            if (rs->m_ref[r] != INFINITY && (is_ctx || cbase <= rs->jr[r]))
+                                rs->m_ref[r] = mine * cl2;
+                        }
+                    }
+                    named_bar_sync(1, 128);
+                }
+                // P of all chunks into registers while PV of the previous tile runs
+                uint32_t pk[4][16];
+                float ymax = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (c < nch) {
+                        uint32_t sr[32];
+                        tmem_ld32(sa + c * 32, sr);
+                        tmem_wait_ld();
+                        vt_chunk(sr, mref_a + c * 128, jr_a + c * 128, key_ok, !is_ctx, cbase + t,
+                                 cl2, pk[c], ymax);
+                    }
+                }
+                const bool hit = ymax > kSlack;
                 // P^T (shared) is read by PV of the previous tile
                 if (it > 0 && !(ok = mbar_wait(bar_pvdone, (it - 1) & 1, abort_flag)))
                     break;
-                const uint32_t sa = tmem + lane_off + TM_S + b * NR;
-                const uint32_t pline = sbase + p.off_p + t * 128;
-                bool hit = false;
-                for (int c = 0; c < nch; ++c) {
-                    uint32_t sr[32];
-                    tmem_ld32(sa + c * 32, sr);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
 #pragma unroll
-                    for (int e2 = 0; e2 < 16; ++e2) {
-                        float pv[2];
+                for (int c = 0; c < 4; ++c) {
+                    if (c < nch) {
+                        const int blk = c >> 1, c0 = (c & 1) * 4;
 #pragma unroll
-                        for (int q2 = 0; q2 < 2; ++q2) {
-                            const int r = c * 32 + e2 * 2 + q2;
-                            const float y = fmaf(__uint_as_float(sr[e2 * 2 + q2]), cl2, -rs->m_ref[r]);
-                            const bool vis = key_ok && (is_ctx || cbase + t <= rs->jr[r]);
-                            hit |= vis && (y > kSlack);
-                            pv[q2] = vis ? fast_exp2(y) : 0.0f;
-                        }
-                        pk[e2] = pack_bf16x2(pv[0], pv[1]);
+                        for (int v = 0; v < 4; ++v)
+                            st_shared_v4(pline + blk * 16384 + (((c0 + v) ^ (t & 7)) << 4),
+                                         pk[c][4 * v], pk[c][4 * v + 1], pk[c][4 * v + 2], pk[c][4 * v + 3]);
                     }
-                    const int blk = c >> 1, c0 = (c & 1) * 4;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        st_shared_v4(pline + blk * 16384 + (((c0 + v) ^ (t & 7)) << 4),
-                                     pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
                 if (__any_sync(0xffffffffu, hit) && lane == 0)
                     rs->flag[it & 1] = 1;
@@ -592,24 +682,15 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                         uint32_t sr[32];
                         tmem_ld32(sa + c * 32, sr);
                         tmem_wait_ld();
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e2 = 0; e2 < 16; ++e2) {
-                            float pv[2];
-#pragma unroll
-                            for (int q2 = 0; q2 < 2; ++q2) {
-                                const int r = c * 32 + e2 * 2 + q2;
-                                const float y = fmaf(__uint_as_float(sr[e2 * 2 + q2]), cl2, -rs->m_ref[r]);
-                                const bool vis = key_ok && (is_ctx || cbase + t <= rs->jr[r]);
-                                pv[q2] = vis ? fast_exp2(y) : 0.0f;
-                            }
-                            pk[e2] = pack_bf16x2(pv[0], pv[1]);
-                        }
+                        uint32_t pq[16];
+                        float dummy = -INFINITY;
+                        vt_chunk(sr, mref_a + c * 128, jr_a + c * 128, key_ok, !is_ctx, cbase + t,
+                                 cl2, pq, dummy);
                         const int blk = c >> 1, c0 = (c & 1) * 4;
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
                             st_shared_v4(pline + blk * 16384 + (((c0 + v) ^ (t & 7)) << 4),
-                                         pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                                         pq[4 * v], pq[4 * v + 1], pq[4 * v + 2], pq[4 * v + 3]);
                     }
                     named_bar_sync(1, 128);
                     if (stid == 0)
@@ -660,9 +741,16 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                         rs->lrow[c * 32 + e] = __uint_as_float(lr[e]);
                 }
             }
-            named_bar_sync(1, 128);
             const int32_t out_row0 = off + s.rb * p.R;
             const int nact = p.HP * kk;                // active rows of this tile
+            if (stid < nact) {
+                const int r = stid;
+                rs->orow[r] = ((int64_t)(out_row0 + r / p.HP) * p.hq + s.hg * p.HP + r % p.HP) * D;
+            }
+            named_bar_sync(1, 128);
+            if (stid < nact)
+                rs->linv[stid] = 1.0f / rs->lrow[stid];
+            named_bar_sync(1, 128);
             if (s.single) {
                 for (int h = 0; h < DH; ++h) {
                     for (int c = 0; c < nch; ++c) {
@@ -672,19 +760,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             const int r = c * 32 + e;
-                            if (r < nact) {
-                                const int64_t orow = (int64_t)(out_row0 + r / p.HP) * p.hq + s.hg * p.HP + r % p.HP;
-                                reinterpret_cast<uint16_t *>(p.out)[orow * D + h * 128 + t] =
-                                    (uint16_t)(pack_bf16x2(__uint_as_float(ro[e]) / rs->lrow[r], 0.0f) & 0xffffu);
-                            }
+                            if (r < nact)
+                                reinterpret_cast<uint16_t *>(p.out)[rs->orow[r] + h * 128 + t] =
+                                    (uint16_t)(pack_bf16x2(__uint_as_float(ro[e]) * rs->linv[r], 0.0f) & 0xffffu);
                         }
                     }
                 }
-                if (stid < nact && p.lse) {
-                    const int r = stid;
-                    const int64_t orow = (int64_t)(out_row0 + r / p.HP) * p.hq + s.hg * p.HP + r % p.HP;
-                    p.lse[orow] = (rs->m_ref[r] + __log2f(rs->lrow[r])) * 0.69314718055994531f;
-                }
+                if (stid < nact && p.lse)
+                    p.lse[rs->orow[stid] / D] = (rs->m_ref[stid] + __log2f(rs->lrow[stid])) * 0.69314718055994531f;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
@@ -723,50 +806,119 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 named_bar_sync(1, 128);
                 if (rs->last) {
                     __threadfence();
-                    // per row: global max and sum over the pieces (threads r < nact)
+                    const int32_t np = cl - cf + 1;
+                    // slot of piece c (the first CTA's piece is its second segment when its
+                    // range started before this pair)
+                    auto slot_of = [&](int32_t c) {
+                        const int64_t cs = vt_cta_start(total, c, ncta);
+                        return 2 * c + ((c == cf && cs < s.u_pair0) ? 1 : 0);
+                    };
+                    // per row: merged max M and sum L over the pieces (threads r < nact)
                     if (stid < nact) {
                         const int r = stid;
                         float M = -INFINITY;
-                        for (int32_t c = cf; c <= cl; ++c) {
-                            const int64_t cs = vt_cta_start(total, c, ncta);
-                            const int32_t sl = 2 * c + ((c == cf && cs < s.u_pair0) ? 1 : 0);
-                            M = fmaxf(M, __ldcg(p.part_ml + (int64_t)sl * kRows + r).x);
+                        for (int32_t c0 = 0; c0 < np; c0 += 8) {
+                            float2 ml[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                ml[q] = (c0 + q < np) ? __ldcg(p.part_ml + (int64_t)slot_of(cf + c0 + q) * kRows + r)
+                                                      : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                M = fmaxf(M, ml[q].x);
                         }
                         float Ls = 0.0f;
-                        for (int32_t c = cf; c <= cl; ++c) {
-                            const int64_t cs = vt_cta_start(total, c, ncta);
-                            const int32_t sl = 2 * c + ((c == cf && cs < s.u_pair0) ? 1 : 0);
-                            const float2 ml = __ldcg(p.part_ml + (int64_t)sl * kRows + r);
-                            Ls += ml.y * fast_exp2(ml.x - M);
+                        for (int32_t c0 = 0; c0 < np; c0 += 8) {
+                            float2 ml[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                ml[q] = (c0 + q < np) ? __ldcg(p.part_ml + (int64_t)slot_of(cf + c0 + q) * kRows + r)
+                                                      : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                Ls += ml[q].y * fast_exp2(ml[q].x - M);
                         }
-                        rs->m_ref[r] = M;          // reused as the merged max
+                        rs->m_ref[r] = M;          // merged max and sum of row r
                         rs->lrow[r] = Ls;
-                        if (p.lse) {
-                            const int64_t orow = (int64_t)(out_row0 + r / p.HP) * p.hq + s.hg * p.HP + r % p.HP;
-                            p.lse[orow] = (M + __log2f(Ls)) * 0.69314718055994531f;
-                        }
+                        if (p.lse)
+                            p.lse[rs->orow[r] / D] = (M + __log2f(Ls)) * 0.69314718055994531f;
                     }
-                    named_bar_sync(1, 128);
-                    // thread = column of d; rows in order, pieces in order
-                    for (int r = 0; r < nact; ++r) {
-                        const float M = rs->m_ref[r], inv = 1.0f / rs->lrow[r];
-                        float acc[DH];
-#pragma unroll
-                        for (int h = 0; h < DH; ++h)
-                            acc[h] = 0.0f;
-                        for (int32_t c = cf; c <= cl; ++c) {
-                            const int64_t cs = vt_cta_start(total, c, ncta);
-                            const int32_t sl = 2 * c + ((c == cf && cs < s.u_pair0) ? 1 : 0);
-                            const float wgt = fast_exp2(__ldcg(p.part_ml + (int64_t)sl * kRows + r).x - M);
-#pragma unroll
-                            for (int h = 0; h < DH; ++h)
-                                acc[h] += wgt * __ldcg(p.part_o + ((int64_t)sl * kRows + r) * D + h * 128 + t);
+                    // weights of up to 8 pieces per pass; thread = 4 consecutive columns of d
+                    // for a set of rows; 4 rows x 4 pieces of float4 loads in flight.  With
+                    // more than 8 pieces the running sum is kept in the first piece's slot.
+                    constexpr int C4 = D / 4;                // float4 columns
+                    constexpr int RGS = 128 / C4;            // row groups
+                    const int col4 = stid % C4, rg = stid / C4;
+                    const int32_t slot0 = slot_of(cf);
+                    for (int32_t c0 = 0; c0 < np; c0 += 8) {
+                        named_bar_sync(1, 128);
+                        const int32_t npc = min(8, np - c0);
+                        if (stid < nact) {
+                            const int r = stid;
+                            const float M = rs->m_ref[r];
+                            for (int q = 0; q < npc; ++q)
+                                rs->wts[q][r] =
+                                    fast_exp2(__ldcg(p.part_ml + (int64_t)slot_of(cf + c0 + q) * kRows + r).x - M);
                         }
-                        const int64_t orow = (int64_t)(out_row0 + r / p.HP) * p.hq + s.hg * p.HP + r % p.HP;
+                        named_bar_sync(1, 128);
+                        int32_t sl[8];
 #pragma unroll
-                        for (int h = 0; h < DH; ++h)
-                            reinterpret_cast<uint16_t *>(p.out)[orow * D + h * 128 + t] =
-                                (uint16_t)(pack_bf16x2(acc[h] * inv, 0.0f) & 0xffffu);
+                        for (int q = 0; q < 8; ++q)
+                            sl[q] = (q < npc) ? slot_of(cf + c0 + q) : slot0;
+                        const bool last_pass = c0 + 8 >= np;
+                        for (int r0 = rg; r0 < nact; r0 += 4 * RGS) {
+                            float4 acc[4];
+#pragma unroll
+                            for (int rr = 0; rr < 4; ++rr) {
+                                acc[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (c0 > 0 && r0 + rr * RGS < nact)   // running sum of earlier passes
+                                    acc[rr] = __ldcg(reinterpret_cast<const float4 *>(
+                                        p.part_o + ((int64_t)slot0 * kRows + r0 + rr * RGS) * D) + col4);
+                            }
+                            for (int q0 = 0; q0 < npc; q0 += 4) {
+                                float4 x[4][4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                                    for (int rr = 0; rr < 4; ++rr) {
+                                        const int r = r0 + rr * RGS;
+                                        x[q][rr] = (q0 + q < npc && r < nact)
+                                            ? __ldcg(reinterpret_cast<const float4 *>(
+                                                  p.part_o + ((int64_t)sl[q0 + q] * kRows + r) * D) + col4)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    }
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                                    for (int rr = 0; rr < 4; ++rr) {
+                                        const int r = r0 + rr * RGS;
+                                        if (q0 + q < npc && r < nact) {
+                                            const float wq = rs->wts[q0 + q][r];
+                                            acc[rr].x += wq * x[q][rr].x;
+                                            acc[rr].y += wq * x[q][rr].y;
+                                            acc[rr].z += wq * x[q][rr].z;
+                                            acc[rr].w += wq * x[q][rr].w;
+                                        }
+                                    }
+                            }
+#pragma unroll
+                            for (int rr = 0; rr < 4; ++rr) {
+                                const int r = r0 + rr * RGS;
+                                if (r >= nact)
+                                    continue;
+                                if (!last_pass) {
+                                    __stcg(reinterpret_cast<float4 *>(p.part_o + ((int64_t)slot0 * kRows + r) * D) + col4,
+                                           acc[rr]);
+                                } else {
+                                    const float inv = 1.0f / rs->lrow[r];
+                                    uint2 pk2;
+                                    pk2.x = pack_bf16x2(acc[rr].x * inv, acc[rr].y * inv);
+                                    pk2.y = pack_bf16x2(acc[rr].z * inv, acc[rr].w * inv);
+                                    *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.out) + rs->orow[r] + col4 * 4) = pk2;
+                                }
+                            }
+                        }
+                        __threadfence_block();
                     }
                     named_bar_sync(1, 128);
                     if (stid == 0)

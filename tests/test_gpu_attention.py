@@ -245,3 +245,14 @@ def test_workspace_reuse_across_sizes_and_mismatch_flag():
     svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots, w=16, ws=ws,
                            k_ctx=bd.k_ctx, v_ctx=bd.v_ctx, cu_ctx=bd.cu_ctx)
     assert ws.read_status() & svp.DEV_WORKSPACE
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_one_long_pair_split_over_many_ctas(paged):
+    # a single (request, KV head) pair of ~40 KV tiles is cut into ~40 pieces, so the
+    # last-arrival merge runs several passes of eight pieces
+    b = wl.make_batch("paged_n64_bf16" if paged else "budget8n_bf16", seed=14, n=1,
+                      lengths=[9], ctx_lengths=[5000], hq=4, hkv=1, d=128, poison=True)
+    out, lse = gpu_verify(to_dev(b))
+    ref_o, ref_l = oracle_verify(b)
+    compare_attention(out, lse, ref_o, ref_l, rows_of(b), torch.bfloat16)
