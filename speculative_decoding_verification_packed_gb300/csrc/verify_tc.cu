@@ -40,13 +40,17 @@ constexpr int kSubBytes = 16384;    // [128 keys][64 d]
 constexpr float kSlack = 32.0f;     // P <= 2^32 (exact in bf16 / fp32 accumulation)
 
 // Shared per-row softmax state (in the misc region).
+constexpr int kReqCache = 256;      // requests whose (offset, context length) sit in smem
+
 struct VtRows {
     float m_ref[128];
     float alpha[128];
-    float red[4][128];
+    union {
+        float red[4][128];   // rare path: per-quarter row maxima
+        float wts[8][128];   // merge: per-piece weight of each row
+    };
     int32_t jr[128];     // candidate index of the row (INT_MAX for padding rows)
     float lrow[128];
-    float wts[8][128];   // combine: per-piece weight of each row
     int64_t orow[128];   // epilogue: output element offset of row r (-1: not a live row)
     float linv[128];     // epilogue: 1 / l of row r
     int32_t flag[2];
@@ -55,7 +59,24 @@ struct VtRows {
     int32_t abort_flag;
     uint32_t tmem;
     int32_t warp_sums[8];
+    int32_t req_off[kReqCache];
+    int32_t req_len[kReqCache];
+    int32_t pslot[256];   // merge: partial slot of each piece (pieces <= CTAs <= 256)
+    int32_t npend;        // merges this CTA owes (it delivered the last piece of a pair)
+    int32_t pend[2][8];   // pair, cf, cl, nact, out_row0, hg, u_pair0 (lo, hi)
 };
+
+__device__ __forceinline__ int32_t rs_req_off(const VtRows *rs, const TcParams &p, int32_t i)
+{
+    return i < kReqCache ? rs->req_off[i] : __ldg(p.cu_slots + i);
+}
+
+__device__ __forceinline__ int32_t rs_req_len(const VtRows *rs, const TcParams &p, int32_t i)
+{
+    if (i < kReqCache)
+        return rs->req_len[i];
+    return p.ctx_len ? __ldg(p.ctx_len + i) : 0;
+}
 
 __device__ __forceinline__ int64_t vt_cta_start(int64_t total, int32_t c, int32_t C)
 {
@@ -112,8 +133,8 @@ __device__ __forceinline__ void vt_units(const TcParams &p, int32_t i, int32_t r
     n_tiles = (L + kVK - 1) / kVK + (cmax + p.CB - 1) / p.CB;
 }
 
-__device__ __forceinline__ void vt_seg(const TcParams &p, const int32_t *prefix, int32_t nq,
-                                       int64_t u, int64_t ue, int64_t cta_s, VtSeg &s)
+__device__ __forceinline__ void vt_seg(const TcParams &p, const VtRows *rs, const int32_t *prefix,
+                                       int32_t nq, int64_t u, int64_t ue, int64_t cta_s, VtSeg &s)
 {
     int32_t lo = 0, hi = nq;
     while (hi - lo > 1) {
@@ -136,7 +157,7 @@ __device__ __forceinline__ void vt_seg(const TcParams &p, const int32_t *prefix,
     s.u_pair0 = prefix[q] + (int64_t)s.hg * per;
     const int64_t seg_end = min(ue, s.u_pair0 + per);
     s.t1 = s.t0 + (int32_t)(seg_end - u);
-    const int32_t L = p.ctx_len ? __ldg(p.ctx_len + s.i) : 0;
+    const int32_t L = rs_req_len(rs, p, s.i);
     s.n_ctx = (L + kVK - 1) / kVK;
     s.first_of_cta = (u == cta_s);
     s.single = (s.t0 == 0 && s.t1 == per);
@@ -216,6 +237,15 @@ __device__ __forceinline__ void vt_chunk(const uint32_t (&sr)[32], uint32_t mref
         pk[e] = pack_bf16x2(fast_exp2(y[2 * e]), fast_exp2(y[2 * e + 1]));
 }
 
+// One contiguous global -> shared copy on the async proxy, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_constant__ TcParams p)
 {
@@ -238,6 +268,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
     auto bar_sfree = [&](int b) { return bar0 + 8u * (20 + b); };
     const uint32_t bar_pfull = bar0 + 8u * 22, bar_pvdone = bar0 + 8u * 23;
     const uint32_t bar_ofree = bar0 + 8u * 24, bar_drain = bar0 + 8u * 25;
+    const uint32_t bar_merge = bar0 + 8u * 26;
 
     VtRows *rs = reinterpret_cast<VtRows *>(smem + p.off_misc);
     volatile int *abort_flag = &rs->abort_flag;
@@ -261,10 +292,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         mbar_init(bar_pvdone, 1);
         mbar_init(bar_ofree, 4);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_merge, 1);
         mbar_fence_init();
         rs->abort_flag = 0;
         rs->flag[0] = rs->flag[1] = 0;
         rs->rescale = 0;
+        rs->npend = 0;
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tm_q);
@@ -298,6 +331,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             vt_units(p, q / p.RB, q % p.RB, nt, bad);
             bad_bits |= bad;
             units = nt * p.HG;
+            const int32_t i = q / p.RB;
+            if (q % p.RB == 0 && i < kReqCache) {
+                rs->req_off[i] = __ldg(p.cu_slots + i);
+                rs->req_len[i] = p.ctx_len ? __ldg(p.ctx_len + i) : 0;
+            }
         }
         int32_t incl = units;
 #pragma unroll
@@ -348,11 +386,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         // fetch a tile's page ids in parallel (shared by its K and V), one tile ahead.
         uint32_t it = 0, nseg = 0, seq = 0;
         bool ok = true;
+        const uint64_t pol_stream = l2_policy_evict_first();   // each KV byte is read once
         for (int64_t u = cta_s; u < cta_e && ok;) {
             VtSeg s;
-            vt_seg(p, prefix, NQ, u, cta_e, cta_s, s);
-            const int32_t off = __ldg(p.cu_slots + s.i);
-            const int32_t L = p.ctx_len ? __ldg(p.ctx_len + s.i) : 0;
+            vt_seg(p, rs, prefix, NQ, u, cta_e, cta_s, s);
+            const int32_t off = rs_req_off(rs, p, s.i);
+            const int32_t L = rs_req_len(rs, p, s.i);
             const int32_t g = (s.hg * p.HP) / p.G;
             const int32_t npages = (L + 15) / 16;
             const int32_t *bt_row = p.paged ? p.block_table + (int64_t)s.i * p.max_pages : nullptr;
@@ -408,16 +447,16 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                             __syncwarp();
                             if (id >= 0) {      // lane pp issues page pp
                                 for (int c = 0; c < 2; ++c)
-                                    tma_load_4d(dst + c * kSubBytes + lane * 2048, mc, bar_full(sl),
-                                                h * 128 + c * 64, 0, g, id);
+                                    tma_load_4d_hint(dst + c * kSubBytes + lane * 2048, mc, bar_full(sl),
+                                                     h * 128 + c * 64, 0, g, id, pol_stream);
                             }
                         } else if (lane == 0) {
                             if (t < s.n_ctx) {
                                 mbar_arrive_expect_tx(bar_full(sl), (uint32_t)kSlotBytes);
                                 const int32_t row = (int32_t)(cctx + (int64_t)t * kVK);
                                 for (int c = 0; c < 2; ++c)
-                                    tma_load_3d(dst + c * kSubBytes, mc, bar_full(sl),
-                                                h * 128 + c * 64, g, row);
+                                    tma_load_3d_hint(dst + c * kSubBytes, mc, bar_full(sl),
+                                                     h * 128 + c * 64, g, row, pol_stream);
                             } else {
                                 const int32_t ct = t - s.n_ctx;
                                 mbar_arrive_expect_tx(bar_full(sl), (uint32_t)(2 * p.CB * 128));
@@ -447,10 +486,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             bool ok = true;
             for (int64_t u = cta_s; u < cta_e && ok;) {
                 VtSeg s;
-                vt_seg(p, prefix, NQ, u, cta_e, cta_s, s);
-                const int32_t off = __ldg(p.cu_slots + s.i);
-                const int32_t k_i = __ldg(p.cu_slots + s.i + 1) - off;
-                const int32_t L = p.ctx_len ? __ldg(p.ctx_len + s.i) : 0;
+                vt_seg(p, rs, prefix, NQ, u, cta_e, cta_s, s);
+                const int32_t off = rs_req_off(rs, p, s.i);
+                const int32_t k_i = (s.i + 1 < kReqCache && s.i + 1 < p.n ? rs->req_off[s.i + 1]
+                                                                          : __ldg(p.cu_slots + s.i + 1)) - off;
+                const int32_t L = rs_req_len(rs, p, s.i);
                 const int32_t kk = min(k_i - s.rb * p.R, p.R);
                 const uint32_t NRs = (uint32_t)((p.HP * kk + 31) / 32 * 32);
                 const uint32_t idesc_s = idesc_bf16_f32(128, NRs, false, false);
@@ -541,10 +581,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         bool ok = true;
         for (int64_t u = cta_s; u < cta_e && ok;) {
             VtSeg s;
-            vt_seg(p, prefix, NQ, u, cta_e, cta_s, s);
-            const int32_t off = __ldg(p.cu_slots + s.i);
-            const int32_t k_i = __ldg(p.cu_slots + s.i + 1) - off;
-            const int32_t L = p.ctx_len ? __ldg(p.ctx_len + s.i) : 0;
+            vt_seg(p, rs, prefix, NQ, u, cta_e, cta_s, s);
+            const int32_t off = rs_req_off(rs, p, s.i);
+            const int32_t k_i = (s.i + 1 < kReqCache && s.i + 1 < p.n ? rs->req_off[s.i + 1]
+                                                                      : __ldg(p.cu_slots + s.i + 1)) - off;
+            const int32_t L = rs_req_len(rs, p, s.i);
             const int32_t kk = min(k_i - s.rb * p.R, p.R);
             const int NRs = (p.HP * kk + 31) / 32 * 32;
             const int nch = NRs / 32;
@@ -774,6 +815,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     mbar_arrive(bar_ofree);
             } else {
                 const int32_t slot = 2 * blockIdx.x + (s.first_of_cta ? 0 : 1);
+                const uint64_t pol_keep = l2_policy_evict_last();   // read back by the merge
                 for (int h = 0; h < DH; ++h) {
                     for (int c = 0; c < nch; ++c) {
                         uint32_t ro[32];
@@ -783,14 +825,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                         for (int e = 0; e < 32; ++e) {
                             const int r = c * 32 + e;
                             if (r < nact)
-                                __stcg(p.part_o + ((int64_t)slot * kRows + r) * D + h * 128 + t,
-                                       __uint_as_float(ro[e]));
+                                st_global_f32_hint(p.part_o + ((int64_t)slot * kRows + r) * D + h * 128 + t,
+                                                   __uint_as_float(ro[e]), pol_keep);
                         }
                     }
                 }
                 if (stid < nact)
-                    __stcg(p.part_ml + (int64_t)slot * kRows + stid,
-                           make_float2(rs->m_ref[stid], rs->lrow[stid]));
+                    st_global_f2_hint(p.part_ml + (int64_t)slot * kRows + stid,
+                                      make_float2(rs->m_ref[stid], rs->lrow[stid]), pol_keep);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
@@ -804,130 +846,121 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     rs->last = (prev == cl - cf) ? 1 : 0;
                 }
                 named_bar_sync(1, 128);
-                if (rs->last) {
-                    __threadfence();
-                    const int32_t np = cl - cf + 1;
-                    // slot of piece c (the first CTA's piece is its second segment when its
-                    // range started before this pair)
-                    auto slot_of = [&](int32_t c) {
-                        const int64_t cs = vt_cta_start(total, c, ncta);
-                        return 2 * c + ((c == cf && cs < s.u_pair0) ? 1 : 0);
-                    };
-                    // per row: merged max M and sum L over the pieces (threads r < nact)
-                    if (stid < nact) {
-                        const int r = stid;
-                        float M = -INFINITY;
-                        for (int32_t c0 = 0; c0 < np; c0 += 8) {
-                            float2 ml[8];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                ml[q] = (c0 + q < np) ? __ldcg(p.part_ml + (int64_t)slot_of(cf + c0 + q) * kRows + r)
-                                                      : make_float2(-INFINITY, 0.0f);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                M = fmaxf(M, ml[q].x);
-                        }
-                        float Ls = 0.0f;
-                        for (int32_t c0 = 0; c0 < np; c0 += 8) {
-                            float2 ml[8];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                ml[q] = (c0 + q < np) ? __ldcg(p.part_ml + (int64_t)slot_of(cf + c0 + q) * kRows + r)
-                                                      : make_float2(-INFINITY, 0.0f);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                Ls += ml[q].y * fast_exp2(ml[q].x - M);
-                        }
-                        rs->m_ref[r] = M;          // merged max and sum of row r
-                        rs->lrow[r] = Ls;
-                        if (p.lse)
-                            p.lse[rs->orow[r] / D] = (M + __log2f(Ls)) * 0.69314718055994531f;
-                    }
-                    // weights of up to 8 pieces per pass; thread = 4 consecutive columns of d
-                    // for a set of rows; 4 rows x 4 pieces of float4 loads in flight.  With
-                    // more than 8 pieces the running sum is kept in the first piece's slot.
-                    constexpr int C4 = D / 4;                // float4 columns
-                    constexpr int RGS = 128 / C4;            // row groups
-                    const int col4 = stid % C4, rg = stid / C4;
-                    const int32_t slot0 = slot_of(cf);
-                    for (int32_t c0 = 0; c0 < np; c0 += 8) {
-                        named_bar_sync(1, 128);
-                        const int32_t npc = min(8, np - c0);
-                        if (stid < nact) {
-                            const int r = stid;
-                            const float M = rs->m_ref[r];
-                            for (int q = 0; q < npc; ++q)
-                                rs->wts[q][r] =
-                                    fast_exp2(__ldcg(p.part_ml + (int64_t)slot_of(cf + c0 + q) * kRows + r).x - M);
-                        }
-                        named_bar_sync(1, 128);
-                        int32_t sl[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            sl[q] = (q < npc) ? slot_of(cf + c0 + q) : slot0;
-                        const bool last_pass = c0 + 8 >= np;
-                        for (int r0 = rg; r0 < nact; r0 += 4 * RGS) {
-                            float4 acc[4];
-#pragma unroll
-                            for (int rr = 0; rr < 4; ++rr) {
-                                acc[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
-                                if (c0 > 0 && r0 + rr * RGS < nact)   // running sum of earlier passes
-                                    acc[rr] = __ldcg(reinterpret_cast<const float4 *>(
-                                        p.part_o + ((int64_t)slot0 * kRows + r0 + rr * RGS) * D) + col4);
-                            }
-                            for (int q0 = 0; q0 < npc; q0 += 4) {
-                                float4 x[4][4];
-#pragma unroll
-                                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                                    for (int rr = 0; rr < 4; ++rr) {
-                                        const int r = r0 + rr * RGS;
-                                        x[q][rr] = (q0 + q < npc && r < nact)
-                                            ? __ldcg(reinterpret_cast<const float4 *>(
-                                                  p.part_o + ((int64_t)sl[q0 + q] * kRows + r) * D) + col4)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                                    }
-#pragma unroll
-                                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                                    for (int rr = 0; rr < 4; ++rr) {
-                                        const int r = r0 + rr * RGS;
-                                        if (q0 + q < npc && r < nact) {
-                                            const float wq = rs->wts[q0 + q][r];
-                                            acc[rr].x += wq * x[q][rr].x;
-                                            acc[rr].y += wq * x[q][rr].y;
-                                            acc[rr].z += wq * x[q][rr].z;
-                                            acc[rr].w += wq * x[q][rr].w;
-                                        }
-                                    }
-                            }
-#pragma unroll
-                            for (int rr = 0; rr < 4; ++rr) {
-                                const int r = r0 + rr * RGS;
-                                if (r >= nact)
-                                    continue;
-                                if (!last_pass) {
-                                    __stcg(reinterpret_cast<float4 *>(p.part_o + ((int64_t)slot0 * kRows + r) * D) + col4,
-                                           acc[rr]);
-                                } else {
-                                    const float inv = 1.0f / rs->lrow[r];
-                                    uint2 pk2;
-                                    pk2.x = pack_bf16x2(acc[rr].x * inv, acc[rr].y * inv);
-                                    pk2.y = pack_bf16x2(acc[rr].z * inv, acc[rr].w * inv);
-                                    *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.out) + rs->orow[r] + col4 * 4) = pk2;
-                                }
-                            }
-                        }
-                        __threadfence_block();
-                    }
-                    named_bar_sync(1, 128);
-                    if (stid == 0)
-                        p.tickets[s.pair] = 0;
+                if (rs->last && stid == 0) {
+                    // this CTA delivered the pair's last piece: merge it after its range,
+                    // when the TMA ring is idle
+                    int32_t *e = rs->pend[rs->npend++];
+                    e[0] = s.pair; e[1] = cf; e[2] = cl; e[3] = nact; e[4] = out_row0; e[5] = s.hg;
+                    e[6] = (int32_t)(s.u_pair0 & 0xffffffff); e[7] = (int32_t)(s.u_pair0 >> 32);
                 }
             }
             named_bar_sync(1, 128);
             ++nseg;
             u += nt;
+        }
+        // ---- merges owed by this CTA: partial slabs -> TMA ring (one bulk copy per
+        // piece), then weights x slabs from shared memory; pieces in order.
+        named_bar_sync(1, 128);
+        const int npend = ok ? rs->npend : 0;
+        uint32_t merge_phase = 0;
+        for (int pi = 0; pi < npend && ok; ++pi) {
+            const int32_t *e = rs->pend[pi];
+            const int32_t pair = e[0], cf = e[1], cl = e[2], nact = e[3], out_row0 = e[4], hg = e[5];
+            const int64_t u_pair0 = (int64_t)(uint32_t)e[6] | ((int64_t)e[7] << 32);
+            const int32_t np = cl - cf + 1;
+            for (int32_t q = stid; q < np; q += 128) {
+                const int32_t c = cf + q;
+                const int64_t cs = vt_cta_start(total, c, ncta);
+                rs->pslot[q] = 2 * c + ((q == 0 && cs < u_pair0) ? 1 : 0);
+            }
+            if (stid < nact) {
+                const int r = stid;
+                rs->orow[r] = ((int64_t)(out_row0 + r / p.HP) * p.hq + hg * p.HP + r % p.HP) * D;
+            }
+            named_bar_sync(1, 128);
+            // per row: merged max M and sum L over the pieces, one online pass
+            if (stid < nact) {
+                const int r = stid;
+                float M = -INFINITY, Ls = 0.0f;
+                for (int32_t c0 = 0; c0 < np; c0 += 8) {
+                    float2 ml[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        ml[q] = (c0 + q < np) ? __ldcg(p.part_ml + (int64_t)rs->pslot[c0 + q] * kRows + r)
+                                              : make_float2(-INFINITY, 0.0f);
+                    float Mb = M;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        Mb = fmaxf(Mb, ml[q].x);
+                    float Lb = (M == -INFINITY) ? 0.0f : Ls * fast_exp2(M - Mb);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (c0 + q < np)
+                            Lb += ml[q].y * fast_exp2(ml[q].x - Mb);
+                    M = Mb;
+                    Ls = Lb;
+                }
+                rs->m_ref[r] = M;
+                rs->linv[r] = 1.0f / Ls;
+                if (p.lse)
+                    p.lse[rs->orow[r] / D] = (M + __log2f(Ls)) * 0.69314718055994531f;
+            }
+            const uint32_t slab = (uint32_t)(((int64_t)nact * D * 4 + 127) / 128 * 128);
+            const int32_t cap_ring = (int32_t)((uint32_t)(nslot * kSlotBytes) / slab);
+            const int32_t cap = cap_ring < 8 ? cap_ring : 8;
+            constexpr int C4 = D / 4;
+            constexpr int RGS = 128 / C4;
+            const int col4 = stid % C4, rg = stid / C4;
+            const int32_t slot0 = rs->pslot[0];
+            for (int32_t c0 = 0; c0 < np && ok; c0 += cap) {
+                const int32_t nb = min(cap, np - c0);
+                named_bar_sync(1, 128);
+                if (stid == 0) {
+                    asm volatile("fence.proxy.async;" ::: "memory");
+                    mbar_arrive_expect_tx(bar_merge, (uint32_t)nb * slab);
+                    for (int q = 0; q < nb; ++q)
+                        bulk_g2s(sbase + p.off_ring + q * slab,
+                                 p.part_o + (int64_t)rs->pslot[c0 + q] * kRows * D, slab, bar_merge);
+                }
+                if (stid < nact) {
+                    const int r = stid;
+                    for (int q = 0; q < nb; ++q)
+                        rs->wts[q][r] = fast_exp2(__ldcg(p.part_ml + (int64_t)rs->pslot[c0 + q] * kRows + r).x -
+                                                  rs->m_ref[r]);
+                }
+                named_bar_sync(1, 128);
+                if (!(ok = mbar_wait(bar_merge, merge_phase & 1, abort_flag)))
+                    break;
+                ++merge_phase;
+                const bool last_pass = c0 + cap >= np;
+                for (int r = rg; r < nact; r += RGS) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (c0 > 0)   // running sum of earlier passes, kept in the first piece's slot
+                        acc = __ldcg(reinterpret_cast<const float4 *>(p.part_o + ((int64_t)slot0 * kRows + r) * D) + col4);
+                    for (int q = 0; q < nb; ++q) {
+                        const float4 x = ld_shared_f4(sbase + p.off_ring + q * slab + (r * D + col4 * 4) * 4);
+                        const float wq = rs->wts[q][r];
+                        acc.x += wq * x.x;
+                        acc.y += wq * x.y;
+                        acc.z += wq * x.z;
+                        acc.w += wq * x.w;
+                    }
+                    if (!last_pass) {
+                        __stcg(reinterpret_cast<float4 *>(p.part_o + ((int64_t)slot0 * kRows + r) * D) + col4, acc);
+                    } else {
+                        const float inv = rs->linv[r];
+                        uint2 pk2;
+                        pk2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+                        pk2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.out) + rs->orow[r] + col4 * 4) = pk2;
+                    }
+                }
+                if (!last_pass)
+                    __threadfence_block();
+            }
+            named_bar_sync(1, 128);
+            if (stid == 0)
+                p.tickets[pair] = 0;
         }
     }
 
@@ -973,7 +1006,7 @@ bool verify_tc_layout(int d, int NR, TcParams &p)
     p.off_q = off; off += q;
     p.off_p = off; off += pt;
     p.off_ones = off; off += 1024;
-    p.off_bar = off; off += 26 * 8;
+    p.off_bar = off; off += 27 * 8;
     off = (off + 15) / 16 * 16;
     p.off_misc = off; off += (int)sizeof(VtRows);
     off = (off + 15) / 16 * 16;
