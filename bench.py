@@ -12,7 +12,10 @@ A step is one pass of the hot path over one batch of the workload:
 The metric is verified candidate rows per second (rows = packed live rows M_live).
 Inputs are resident in HBM when the timed region starts; consecutive steps rotate over
 several independent input sets whose total footprint exceeds twice the L2 size, so a
-step never finds its KV stream in L2.  Rank 0 prints one JSON line.
+step never finds its KV stream in L2.  Each launch of a step is replayed from a CUDA
+graph captured once per input set (the C-ABI calls are capture-safe, as a serving step
+would replay them), so the timed region holds no host work; CUDA events around every
+launch give the per-kernel durations used for the roofline.  Rank 0 prints one JSON line.
 
 --impl reference times the fp64 CPU oracle (the reference arm of this repository) on a
 bounded sample of the same workload on the host cores.
@@ -53,8 +56,8 @@ WORKLOAD_TEXT = {
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="full_width_bf16", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
@@ -109,7 +112,7 @@ def measured_peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -124,7 +127,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -236,30 +239,50 @@ def n_sets_for(b0) -> int:
     return max(1, min(8, math.ceil(2 * L2_BYTES / per) + 1)) if per < 4 * L2_BYTES else 1
 
 
-def timed_run(sets, steps, warmup, svp, tile_mode=None, clocks=None):
-    """K steps rotating over the input sets; per-launch device times via events."""
+def capture_step(plan, stream):
+    """One CUDA graph per launch of the step (replayed in order inside the timed loop)."""
     import torch
-    plans = [build_step(b, svp, tile_mode)[0] for b in sets]
-    stream = torch.cuda.current_stream()
-    for w in range(warmup):
-        for _, fn in plans[w % len(plans)]:
-            fn()
+    with torch.cuda.stream(stream):
+        for _, fn in plan:
+            fn()                      # first use: workspace signature, lazy init
     torch.cuda.synchronize()
-    nl = len(plans[0])
+    graphs = []
+    for name, fn in plan:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs.append((name, g))
+    torch.cuda.synchronize()
+    return graphs
+
+
+def timed_run(sets, steps, warmup, svp, tile_mode=None, clocks=None):
+    """K steps rotating over the input sets, each step replayed from captured graphs
+    (no host work inside the timed region); per-launch device times from events
+    recorded on the stream around each launch."""
+    import torch
+    stream = torch.cuda.current_stream()
+    plans = [build_step(b, svp, tile_mode)[0] for b in sets]
+    graphs = [capture_step(pl, torch.cuda.Stream()) for pl in plans]
+    if clocks:
+        clocks.start()          # sampling spans the warm-up and the timed region
+        time.sleep(0.2)
+    for w in range(warmup):
+        for _, g in graphs[w % len(graphs)]:
+            g.replay()
+    torch.cuda.synchronize()
+    nl = len(graphs[0])
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(nl)] for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    if clocks:
-        clocks.start()
-        time.sleep(0.3)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     t0.record(stream)
     for s in range(steps):
-        for li, (_, fn) in enumerate(plans[s % len(plans)]):
+        for li, (_, g) in enumerate(graphs[s % len(graphs)]):
             ev[s][li][0].record(stream)
-            fn()
+            g.replay()
             ev[s][li][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -268,7 +291,7 @@ def timed_run(sets, steps, warmup, svp, tile_mode=None, clocks=None):
     total_ms = t0.elapsed_time(t1)
     per_launch = [statistics.mean(ev[s][li][0].elapsed_time(ev[s][li][1]) for s in range(steps))
                   for li in range(nl)]
-    names = [n for n, _ in plans[0]]
+    names = [n for n, _ in graphs[0]]
     return total_ms, dict(zip(names, per_launch)), clk, wall, steps * nl
 
 
@@ -277,7 +300,7 @@ def e2e_run(sets, steps, warmup, svp):
     inputs host->device, runs the step, and reads the outputs back."""
     import torch
     hosts = []
-    for b in sets:
+    for b in sets[:1]:        # one batch shape: every step re-uploads the same inputs
         h = {}
         for name in ("q", "k_new", "v_new", "ctx_len", "cu_slots", "k_ctx", "v_ctx", "cu_ctx",
                      "k_cache", "v_cache", "block_table", "tokens", "target_logits",
@@ -316,32 +339,35 @@ def e2e_run(sets, steps, warmup, svp):
     return t0.elapsed_time(t1), h2d, d2h
 
 
-def traffic_record(workload: str):
-    """ncu DRAM bytes per launch of the attention kernel from profiles/, if the kernel
-    source is unchanged since the capture (else None)."""
+def traffic_record(workload: str, algorithmic_bytes: float):
+    """DRAM bytes per launch of the attention kernel from the ncu capture summarised in
+    profiles/attn_traffic.json, scaled from the captured launch to this launch's
+    algorithmic bytes (traffic grows with the KV tiles streamed); None when the kernel
+    source changed since the capture or no capture exists for the workload."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "attn_traffic.json")
-    src = os.path.join(ROOT, "speculative_decoding_verification_packed_gb300", "csrc", "attn_tc.cu")
+    src = os.path.join(ROOT, "speculative_decoding_verification_packed_gb300", "csrc", "verify_tc.cu")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     r = rec.get(workload)
-    if not r or r.get("attn_tc_sha") != h:
+    if not r or r.get("kernel_src_sha") != h:
         return None
-    return r.get("dram_bytes_per_launch")
+    return int(r["traffic_over_algorithmic"] * algorithmic_bytes)
 
 
 def cpu_baseline(name, seed, budget_s=15.0):
-    """The fp64 oracle timed on this host's cores on a bounded sample of the workload."""
+    """The fp64 oracle timed on this host's cores on a bounded sample of the workload
+    (whole requests, all heads, until about budget_s seconds of CPU work)."""
     import torch
     import oracle
     from speculative_decoding_verification_packed_gb300 import workloads as wl
     threads = os.cpu_count() or 1
     b = wl.make_batch(name, seed=seed, device="cpu", with_logits=False)
     cu = b.cu_slots.tolist()
-    order = list(range(b.n))
+    order = list(range(b.n)) * 64          # whole batch, repeated until the time budget
     done_rows, t_used, reqs = 0, 0.0, []
     for i in order:
         t0 = time.perf_counter()
@@ -359,8 +385,9 @@ def cpu_baseline(name, seed, budget_s=15.0):
         if t_used >= budget_s:
             break
     return {"value": done_rows / t_used, "unit": "rows/s", "cores": threads, "kind": "oracle",
-            "sample": f"{len(reqs)} of {b.n} requests ({done_rows} rows, all heads) of {name}, "
-                      f"seed {seed}, fp64 C oracle, {t_used:.1f} s"}
+            "sample": f"{len(reqs)} request passes over the {b.n}-request batch in order "
+                      f"({done_rows} rows, all {b.hq} heads) of {name}, seed {seed}, fp64 C "
+                      f"oracle, {t_used:.1f} s"}
 
 
 def run_ours(args):
@@ -394,7 +421,7 @@ def run_ours(args):
     kvb = statistics.mean(kv_bytes(b) for b in sets)
     attn_ms = per_launch["attn"]
     achieved = kvb / (attn_ms / 1e3) / 1e9
-    tr = traffic_record(args.workload)
+    tr = traffic_record(args.workload, kvb)
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -407,7 +434,7 @@ def run_ours(args):
                          f"(> 2x the 129 MB L2)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "traffic": tr, "kernel": "attn_tc_kernel",
+                     "traffic": tr, "kernel": "verify_tc_kernel",
                      "algorithmic_bytes_per_launch": int(kvb), "launch_us": round(attn_ms * 1e3, 2),
                      "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
@@ -424,10 +451,9 @@ def run_ours(args):
         result["margin_accept_gbs"] = round(tb / (per_launch["margin_accept"] / 1e3) / 1e9, 1)
 
     # end to end through the public API with host buffers
-    e2e_ms, h2d, d2h = e2e_run(sets[:2], max(3, args.steps // 5), 3, svp)
     e2e_steps = max(3, args.steps // 5)
-    e2e_rows = sum(int(sets[s % 2].cu_slots[-1]) for s in range(e2e_steps)) if nsets > 1 else \
-        e2e_steps * int(sets[0].cu_slots[-1])
+    e2e_ms, h2d, d2h = e2e_run(sets[:1], e2e_steps, 3, svp)
+    e2e_rows = e2e_steps * int(sets[0].cu_slots[-1])
     result["e2e"] = {"value": round(e2e_rows / (e2e_ms / 1e3), 1), "unit": "rows/s",
                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                      "note": "all step inputs (incl. the KV context) copied from pinned host "
@@ -436,9 +462,9 @@ def run_ours(args):
     if not args.no_extras and rank == 0:
         extras = {}
         # contrast: fixed 128-row tile, same inputs, same N
-        fx_ms, fx_pl, _, _, _ = timed_run(sets, max(5, args.steps // 2), 3, svp,
-                                          tile_mode=svp.TILE_FIXED128)
-        fx_rows = sum(int(sets[s % nsets].cu_slots[-1]) for s in range(max(5, args.steps // 2)))
+        fx_steps = max(5, min(200, args.steps // 4))
+        fx_ms, fx_pl, _, _, _ = timed_run(sets, fx_steps, 3, svp, tile_mode=svp.TILE_FIXED128)
+        fx_rows = sum(int(sets[s % nsets].cu_slots[-1]) for s in range(fx_steps))
         extras["fixed128_contrast"] = {
             "rows_per_s": round(fx_rows / (fx_ms / 1e3), 1),
             "kv_gbs": round(kvb / (fx_pl["attn"] / 1e3) / 1e9, 1),
@@ -449,7 +475,7 @@ def run_ours(args):
             osets = make_sets(other, 1, args.seed, dev)
             n2 = n_sets_for(osets[0])
             osets += make_sets(other, n2 - 1, args.seed + 1, dev)
-            st = max(5, args.steps // 5)
+            st = max(5, min(100, args.steps // 20))
             oms, opl, _, _, _ = timed_run(osets, st, 3, svp)
             orows = sum(int(osets[s % n2].cu_slots[-1]) for s in range(st))
             okv = statistics.mean(kv_bytes(b) for b in osets)
@@ -517,28 +543,29 @@ def run_reference(args):
                cache_strides=b.cache_strides) if b.paged else
           dict(k_ctx=b.k_ctx, v_ctx=b.v_ctx, cu_ctx=b.cu_ctx))
 
-    # one step = the request with the shortest context (a bounded sample of the batch)
-    i = min(range(b.n), key=lambda j: (int(b.ctx_len[j]), j))
-
-    def step():
+    # step s = request s mod n (all heads): the batch in order, one request per step,
+    # so that a full cycle of steps is the whole workload
+    def step(s):
+        i = s % b.n
         oracle.attention(b.q, b.k_new, b.v_new, b.ctx_len, b.cu_slots, hkv=b.hkv, scale=b.scale,
                          requests=[i], threads=threads, **kw)
         return cu[i + 1] - cu[i]
 
-    for _ in range(args.warmup):
-        step()
+    for w in range(args.warmup):
+        step(w)
     t0 = time.perf_counter()
     rows = 0
-    for _ in range(args.steps):
-        rows += step()
+    steps = min(args.steps, 3 * b.n)
+    for k in range(steps):
+        rows += step(k)
     dt = time.perf_counter() - t0
     value = rows / dt
-    sample = (f"per step: request {i} of {args.workload} (ctx {int(b.ctx_len[i])}, "
-              f"{cu[i + 1] - cu[i]} rows, all {b.hq} heads), fp64 C oracle")
+    sample = (f"{steps} steps, step s = request s mod {b.n} of {args.workload} (all {b.hq} "
+              f"heads), fp64 C oracle")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "rows/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "description": WORKLOAD_TEXT[args.workload]},
         "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": threads,
