@@ -220,6 +220,29 @@ svp_status svp_margin_accept(const void *logits, int64_t row_stride, int32_t m_c
                              float *top1, float *top2, float *margin, int32_t *accept_len,
                              int32_t *next_token, void *ws, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------------------------- */
+/* Allocation-free variant of svp_margin_accept.  The pages describe no such call; it   */
+/* exists for callers that cannot allocate device memory: code running inside a memory  */
+/* pool or host framework that owns every device allocation, and paths where a          */
+/* cudaMalloc (and the synchronisation it may cause) is not acceptable.                 */
+/*                                                                                      */
+/* Arguments, outputs and results are those of svp_margin_accept, without the workspace.*/
+/* The scratch is a fixed 2 MiB array inside the library, held by every GPU that loads  */
+/* the library until the process exits; sizes whose workspace                           */
+/* (svp_margin_accept_workspace_size) exceeds 2 MiB return SVP_EWORKSPACE and nothing   */
+/* is enqueued.  The first call on each device (with that device current) looks up the  */
+/* array's device address and clears it once (cudaGetSymbolAddress, cudaMemset; no      */
+/* allocation), so make that first call before capturing any stream.  All calls share   */
+/* the one array: calls that overlap on the GPU (other streams, other host threads)     */
+/* race and must be serialised by the caller.  The kernel leaves the array zeroed.      */
+/* Device-side metadata errors are not reported through a status word in this variant:  */
+/* invalid cu_slots leave every row and request unwritten.  Allocates nothing.          */
+svp_status svp_margin_accept_noalloc(const void *logits, int64_t row_stride, int32_t m_cap,
+                                     int32_t vocab, svp_dtype dtype, const int32_t *tokens,
+                                     const int32_t *cu_slots, int32_t n, int32_t *top1_idx,
+                                     float *top1, float *top2, float *margin,
+                                     int32_t *accept_len, int32_t *next_token, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

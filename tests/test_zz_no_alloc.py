@@ -1,0 +1,88 @@
+"""The allocation-free margin + accept entry point (svp_margin_accept_noalloc).
+
+Some callers cannot allocate device memory (a host framework that owns every device
+allocation, or a path where cudaMalloc is not allowed); this entry point keeps its scratch
+in a fixed array inside the library.  The test calls it through the C ABI twice in a row
+and checks every output against svp_margin_accept (with its own workspace), bit for bit
+as in the other margin/accept tests.  This file is collected last on purpose.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_verification_packed_gb300 as svp
+from speculative_decoding_verification_packed_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc_fn():
+    L = svp.lib()
+    fn = L.svp_margin_accept_noalloc
+    vp = ctypes.c_void_p
+    fn.restype = ctypes.c_int
+    fn.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int, vp, vp,
+                   ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp]
+    return fn
+
+
+def _outs(m_cap, n):
+    return (torch.full((m_cap,), -7, dtype=torch.int32, device="cuda"),
+            torch.full((m_cap,), float("nan"), device="cuda"),
+            torch.full((m_cap,), float("nan"), device="cuda"),
+            torch.full((m_cap,), float("nan"), device="cuda"),
+            torch.full((n,), -7, dtype=torch.int32, device="cuda"),
+            torch.full((n,), -7, dtype=torch.int32, device="cuda"))
+
+
+def _call_noalloc(fn, logits, tokens, cu, outs):
+    m_cap, vocab = logits.shape
+    n = cu.shape[0] - 1
+    code = svp.SVP_BF16 if logits.dtype == torch.bfloat16 else svp.SVP_F32
+    return fn(logits.data_ptr(), vocab, m_cap, vocab, code, tokens.data_ptr(), cu.data_ptr(), n,
+              outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), outs[3].data_ptr(),
+              outs[4].data_ptr(), outs[5].data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+def _same(a, b):
+    for x, y in zip(a, b):
+        x, y = x.cpu(), y.cpu()
+        if x.dtype == torch.float32:
+            xb, yb = x.view(torch.int32), y.view(torch.int32)
+            both_nan = torch.isnan(x) & torch.isnan(y)
+            assert bool(((xb == yb) | both_nan).all())
+        else:
+            assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("case", ["tiny_fp32", "wide_vocab_bf16"])
+def test_noalloc_matches_workspace_entry_point_twice(case):
+    if case == "tiny_fp32":
+        b = wl.make_batch("tiny_fp32", seed=3, poison=True)
+    else:
+        b = wl.make_batch("wide_gqa_bf16", seed=5, n=12, hq=1, hkv=1, d=64,
+                          ctx_lengths=[0] * 12, lengths=[7, 1, 3, 7, 7, 2, 7, 0, 5, 7, 7, 4],
+                          m_cap=64)
+    logits = b.target_logits.cuda()
+    tokens = b.tokens.cuda()
+    cu = b.cu_slots.cuda()
+    m_cap, n = logits.shape[0], cu.shape[0] - 1
+    ref = svp.margin_accept(logits, tokens, cu, outs=_outs(m_cap, n))
+    fn = _noalloc_fn()
+    for _ in range(2):                      # two calls in a row share the fixed scratch
+        outs = _outs(m_cap, n)
+        assert _call_noalloc(fn, logits, tokens, cu, outs) == svp.SVP_OK
+        torch.cuda.synchronize()
+        _same(outs, ref)
+    live = int(b.cu_slots[-1])
+    assert (outs[0][live:].cpu() == -7).all()          # rows past cu_slots[n] untouched
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    fn = _noalloc_fn()
+    # 8192 rows x 262144 vocabulary needs far more than the fixed 2 MiB of scratch; the
+    # call is refused on the host before anything is enqueued (pointers never touched)
+    rc = fn(16, 262144, 8192, 262144, svp.SVP_BF16, 16, 16, 64, 16, 16, 16, 16, 16, 16, None)
+    assert rc == svp.SVP_EWORKSPACE
