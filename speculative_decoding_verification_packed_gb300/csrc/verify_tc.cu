@@ -266,9 +266,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
     const uint32_t bar_qfull = bar0 + 8u * 16, bar_qempty = bar0 + 8u * 17;
     auto bar_sfull = [&](int b) { return bar0 + 8u * (18 + b); };
     auto bar_sfree = [&](int b) { return bar0 + 8u * (20 + b); };
-    const uint32_t bar_pfull = bar0 + 8u * 22, bar_pvdone = bar0 + 8u * 23;
-    const uint32_t bar_ofree = bar0 + 8u * 24, bar_drain = bar0 + 8u * 25;
-    const uint32_t bar_merge = bar0 + 8u * 26;
+    auto bar_pfull = [&](int b) { return bar0 + 8u * (22 + b); };    // per P buffer
+    auto bar_pvdone = [&](int b) { return bar0 + 8u * (24 + b); };   // per P buffer
+    const uint32_t bar_ofree = bar0 + 8u * 26, bar_drain = bar0 + 8u * 27;
+    const uint32_t bar_merge = bar0 + 8u * 28;
+    const int nP = p.nP;                                          // P buffers (1 or 2)
+    const uint32_t PBYTES = (uint32_t)((NR + 63) / 64) * 16384u;
 
     VtRows *rs = reinterpret_cast<VtRows *>(smem + p.off_misc);
     volatile int *abort_flag = &rs->abort_flag;
@@ -288,8 +291,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             mbar_init(bar_sfull(b), 1);
             mbar_init(bar_sfree(b), 4);
         }
-        mbar_init(bar_pfull, 4);
-        mbar_init(bar_pvdone, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_pfull(b), 4);
+            mbar_init(bar_pvdone(b), 1);
+        }
         mbar_init(bar_ofree, 4);
         mbar_init(bar_drain, 1);
         mbar_init(bar_merge, 1);
@@ -500,68 +505,94 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     break;
                 tc_fence_after();
                 const int32_t nt = s.t1 - s.t0;
-                for (int32_t k = 0; k <= nt && ok; ++k) {
-                    if (k < nt) {
-                        const uint32_t itk = it + k;
+                // Issue S^T of tile kS and PV of tile kP as soon as each is ready (polling),
+                // so a PV never waits behind the next tile's K load.  S runs at most two
+                // tiles ahead (two S buffers).
+                int32_t kS = 0, kP = 0;
+                bool ofree_ok = (nseg == 0);
+                uint32_t idle = 0;
+                uint64_t idle_t0 = 0;
+                while (kP < nt) {
+                    bool did = false;
+                    if (kS < nt && kS < kP + 2) {
+                        const uint32_t itk = it + kS;
                         const int b = itk & 1;
-                        if (!(ok = mbar_wait(bar_sfree(b), ((itk >> 1) & 1) ^ 1, abort_flag)))
-                            break;
-                        for (int h = 0; h < DH && ok; ++h) {
+                        bool ready = mbar_test_wait(bar_sfree(b), ((itk >> 1) & 1) ^ 1);
+                        for (int h = 0; h < DH && ready; ++h) {
                             const uint32_t sq = itk * 2 * DH + h;
-                            ok = mbar_wait(bar_full(sq % nslot), (sq / nslot) & 1, abort_flag);
+                            ready = mbar_test_wait(bar_full(sq % nslot), (sq / nslot) & 1);
                         }
-                        if (!ok)
-                            break;
-                        tc_fence_after();
-                        for (int h = 0; h < DH; ++h) {
-                            const uint32_t ka = sbase + p.off_ring + ((itk * 2 * DH + h) % nslot) * kSlotBytes;
-                            for (int ks = 0; ks < 8; ++ks) {
-                                const uint32_t a = ka + (ks >> 2) * kSubBytes + (ks & 3) * 32;
-                                const uint32_t bq = sbase + p.off_q + (2 * h + (ks >> 2)) * QSUB + (ks & 3) * 32;
-                                tc_mma_ss(tmem + TM_S + b * NR, sw128_desc(a, 16, 1024),
-                                          sw128_desc(bq, 16, 1024), idesc_s, (h | ks) ? 1u : 0u);
+                        if (ready) {
+                            tc_fence_after();
+                            for (int h = 0; h < DH; ++h) {
+                                const uint32_t ka = sbase + p.off_ring + ((itk * 2 * DH + h) % nslot) * kSlotBytes;
+                                for (int ks = 0; ks < 8; ++ks) {
+                                    const uint32_t a = ka + (ks >> 2) * kSubBytes + (ks & 3) * 32;
+                                    const uint32_t bq = sbase + p.off_q + (2 * h + (ks >> 2)) * QSUB + (ks & 3) * 32;
+                                    tc_mma_ss(tmem + TM_S + b * NR, sw128_desc(a, 16, 1024),
+                                              sw128_desc(bq, 16, 1024), idesc_s, (h | ks) ? 1u : 0u);
+                                }
+                            }
+                            tc_commit(bar_sfull(b));
+                            for (int h = 0; h < DH; ++h)
+                                tc_commit(bar_empty((itk * 2 * DH + h) % nslot));
+                            if (kS == nt - 1)
+                                tc_commit(bar_qempty);   // Q no longer read by this segment
+                            ++kS;
+                            did = true;
+                        }
+                    }
+                    if (kP < kS) {
+                        const uint32_t itp = it + kP;
+                        const int pb = (int)(itp % (uint32_t)nP);
+                        if (!ofree_ok)
+                            ofree_ok = mbar_test_wait(bar_ofree, (nseg - 1) & 1);
+                        bool ready = (kP > 0 || ofree_ok) &&
+                                     mbar_test_wait(bar_pfull(pb), (itp / nP) & 1);
+                        for (int h = 0; h < DH && ready; ++h) {
+                            const uint32_t sq = itp * 2 * DH + DH + h;
+                            ready = mbar_test_wait(bar_full(sq % nslot), (sq / nslot) & 1);
+                        }
+                        if (ready) {
+                            tc_fence_after();
+                            const int32_t t = s.t0 + kP;
+                            const int32_t kv = vt_kvalid(p, s, t, L, k_i);
+                            const int32_t k16 = (kv + 15) / 16;
+                            const uint32_t pbase = sbase + p.off_p + pb * PBYTES;
+                            for (int h = 0; h < DH; ++h) {
+                                const uint32_t va = sbase + p.off_ring + ((itp * 2 * DH + DH + h) % nslot) * kSlotBytes;
+                                for (int ks = 0; ks < k16; ++ks)
+                                    tc_mma_ss(tmem + TM_O + h * NR, sw128_desc(va + ks * 2048, kSubBytes, 1024),
+                                              sw128_desc(pbase + ks * 2048, 16384, 1024), idesc_o,
+                                              (kP == 0 && ks == 0) ? 0u : 1u);
+                            }
+                            for (int ks = 0; ks < k16; ++ks)
+                                tc_mma_ss(tmem + TM_L, sw128_desc(sbase + p.off_ones, 16, 0),
+                                          sw128_desc(pbase + ks * 2048, 16384, 1024), idesc_l,
+                                          (kP == 0 && ks == 0) ? 0u : 1u);
+                            tc_commit(bar_pvdone(pb));
+                            for (int h = 0; h < DH; ++h)
+                                tc_commit(bar_empty((itp * 2 * DH + DH + h) % nslot));
+                            ++kP;
+                            did = true;
+                        }
+                    }
+                    if (did) {
+                        idle = 0;
+                    } else {
+                        if (idle++ == 0)
+                            idle_t0 = global_ns();
+                        if ((idle & 255u) == 0) {
+                            if (*abort_flag || global_ns() - idle_t0 > kWaitLimitNs) {
+                                *abort_flag = 1;
+                                ok = false;
+                                break;
                             }
                         }
-                        tc_commit(bar_sfull(b));
-                        for (int h = 0; h < DH; ++h)
-                            tc_commit(bar_empty((itk * 2 * DH + h) % nslot));
-                        if (k == nt - 1)
-                            tc_commit(bar_qempty);
-                    }
-                    if (k > 0) {
-                        const uint32_t itp = it + k - 1;
-                        const int32_t t = s.t0 + k - 1;
-                        const int32_t kv = vt_kvalid(p, s, t, L, k_i);
-                        const int32_t k16 = (kv + 15) / 16;
-                        if (k == 1 && nseg > 0 &&
-                            !(ok = mbar_wait(bar_ofree, (nseg - 1) & 1, abort_flag)))
-                            break;
-                        if (!(ok = mbar_wait(bar_pfull, itp & 1, abort_flag)))
-                            break;
-                        for (int h = 0; h < DH && ok; ++h) {
-                            const uint32_t sq = itp * 2 * DH + DH + h;
-                            ok = mbar_wait(bar_full(sq % nslot), (sq / nslot) & 1, abort_flag);
-                        }
-                        if (!ok)
-                            break;
-                        tc_fence_after();
-                        const uint32_t pb = sbase + p.off_p;
-                        for (int h = 0; h < DH; ++h) {
-                            const uint32_t va = sbase + p.off_ring + ((itp * 2 * DH + DH + h) % nslot) * kSlotBytes;
-                            for (int ks = 0; ks < k16; ++ks)
-                                tc_mma_ss(tmem + TM_O + h * NR, sw128_desc(va + ks * 2048, kSubBytes, 1024),
-                                          sw128_desc(pb + ks * 2048, 16384, 1024), idesc_o,
-                                          (k == 1 && ks == 0) ? 0u : 1u);
-                        }
-                        for (int ks = 0; ks < k16; ++ks)
-                            tc_mma_ss(tmem + TM_L, sw128_desc(sbase + p.off_ones, 16, 0),
-                                      sw128_desc(pb + ks * 2048, 16384, 1024), idesc_l,
-                                      (k == 1 && ks == 0) ? 0u : 1u);
-                        tc_commit(bar_pvdone);
-                        for (int h = 0; h < DH; ++h)
-                            tc_commit(bar_empty((itp * 2 * DH + DH + h) % nslot));
                     }
                 }
+                if (!ok)
+                    break;
                 it += nt;
                 ++nseg;
                 u += nt;
@@ -609,7 +640,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     break;
                 tc_fence_after();
                 const uint32_t sa = tmem + lane_off + TM_S + b * NR;
-                const uint32_t pline = sbase + p.off_p + t * 128;
+                const uint32_t pline = sbase + p.off_p + (it % (uint32_t)nP) * PBYTES + t * 128;
                 const uint32_t mref_a = smem_u32(rs->m_ref), jr_a = smem_u32(rs->jr);
                 if (k == 0) {
                     // seed the reference of every live row with the score of key 0 of
@@ -648,8 +679,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     }
                 }
                 const bool hit = ymax > kSlack;
-                // P^T (shared) is read by PV of the previous tile
-                if (it > 0 && !(ok = mbar_wait(bar_pvdone, (it - 1) & 1, abort_flag)))
+                // this P buffer is read by PV of tile it - nP
+                if (it >= (uint32_t)nP &&
+                    !(ok = mbar_wait(bar_pvdone(it % nP), ((it - nP) / nP) & 1, abort_flag)))
                     break;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -702,8 +734,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     }
                     named_bar_sync(1, 128);
                     if (rs->rescale) {
-                        // O^T halves and l^T: column r scaled by alpha[r] (PV of the
-                        // previous tile is complete: waited above)
+                        // O^T halves and l^T: column r scaled by alpha[r], once PV of the
+                        // previous tile is complete
+                        if (!(ok = mbar_wait(bar_pvdone((it - 1) % nP), ((it - 1) / nP) & 1, abort_flag)))
+                            break;
+                        tc_fence_after();
                         for (int m = 0; m <= DH; ++m) {
                             const uint32_t base = tmem + lane_off + (m < DH ? TM_O + m * NR : TM_L);
                             for (int c = 0; c < nch; ++c) {
@@ -761,14 +796,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar_pfull);
+                    mbar_arrive(bar_pfull(it % nP));
                 if (!ok)
                     break;
             }
             if (!ok)
                 break;
             // ---- epilogue: O^T, l^T complete after the last PV of the segment
-            if (!(ok = mbar_wait(bar_pvdone, (it - 1) & 1, abort_flag)))
+            if (!(ok = mbar_wait(bar_pvdone((it - 1) % nP), ((it - 1) / nP) & 1, abort_flag)))
                 break;
             tc_fence_after();
             // row sums: every lane of l^T holds l for each column
@@ -997,16 +1032,27 @@ svp_status verify_tc_launch(const TcParams &p, int d, int grid, cudaStream_t str
 }
 
 // Shared-memory layout of verify_tc_kernel for a tile of NR rows (host helper).
+static bool verify_tc_layout_np(int d, int NR, int nP, TcParams &p);
+
 bool verify_tc_layout(int d, int NR, TcParams &p)
+{
+    // two P buffers when the ring keeps enough slots, else one
+    if (verify_tc_layout_np(d, NR, 2, p) && p.nslot >= (d == 128 ? 5 : 4))
+        return true;
+    return verify_tc_layout_np(d, NR, 1, p);
+}
+
+static bool verify_tc_layout_np(int d, int NR, int nP, TcParams &p)
 {
     const int budget = 227 * 1024;
     const int q = (d / 64) * NR * 128;
-    const int pt = ((NR + 63) / 64) * 16384;
+    const int pt = nP * ((NR + 63) / 64) * 16384;
+    p.nP = nP;
     int off = 0;
     p.off_q = off; off += q;
     p.off_p = off; off += pt;
     p.off_ones = off; off += 1024;
-    p.off_bar = off; off += 27 * 8;
+    p.off_bar = off; off += 29 * 8;
     off = (off + 15) / 16 * 16;
     p.off_misc = off; off += (int)sizeof(VtRows);
     off = (off + 15) / 16 * 16;
