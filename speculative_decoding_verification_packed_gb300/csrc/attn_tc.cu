@@ -415,12 +415,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                         tc_fence_after();
                         const uint32_t idesc_s = idesc_bf16_f32(kRows, keys, false, false);
                         const uint32_t kbase = sbase + C::OFF_KV + st * C::STAGE;
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t qa = sbase + C::OFF_Q + (ks >> 2) * C::QSUB + (ks & 3) * 32;
-                            const uint32_t ka = kbase + (ks >> 2) * C::SUB + (ks & 3) * 32;
-                            tc_mma_ss(tmem + C::TMEM_S + b * kBN, sw128_desc(qa, 16, 1024),
-                                      sw128_desc(ka, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
-                        }
+                        // descriptors formed once; a 16-byte step is +1 in the address field
+                        const uint64_t qd = sw128_desc(sbase + C::OFF_Q, 16, 1024);
+                        const uint64_t kd = sw128_desc(kbase, 16, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            tc_mma_ss(tmem + C::TMEM_S + b * kBN,
+                                      qd + (uint64_t)((ks >> 2) * (C::QSUB >> 4) + (ks & 3) * 2),
+                                      kd + (uint64_t)((ks >> 2) * (C::SUB >> 4) + (ks & 3) * 2), idesc_s,
+                                      ks > 0 ? 1u : 0u);
                         tc_commit(bar_sfull(b));
                         if (k == nt - 1)
                             tc_commit(bar_qempty);   // Q no longer read by this segment
@@ -437,13 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                             break;
                         tc_fence_after();
                         const uint32_t vbase = sbase + C::OFF_KV + st * C::STAGE + C::KV_BYTES;
-                        for (int ks = 0; ks < keys / 16; ++ks) {
-                            const uint32_t pa = sbase + C::OFF_P + ks * 32;
-                            const uint32_t va = vbase + ks * 2048;
-                            tc_mma_ss(tmem + C::TMEM_O, sw128_desc(pa, 16, 1024),
-                                      sw128_desc(va, C::SUB, 1024), idesc_pv,
-                                      (k == 1 && ks == 0) ? 0u : 1u);
-                        }
+                        const uint64_t pd = sw128_desc(sbase + C::OFF_P, 16, 1024);
+                        const uint64_t vd = sw128_desc(vbase, C::SUB, 1024);
+                        const uint32_t acc0 = k == 1 ? 0u : 1u;
+                        const int nks = keys / 16;
+#pragma unroll
+                        for (int ks = 0; ks < kBN / 16; ++ks)
+                            if (ks < nks)
+                                tc_mma_ss(tmem + C::TMEM_O, pd + (uint64_t)(ks * 2), vd + (uint64_t)(ks * 128),
+                                          idesc_pv, ks ? 1u : acc0);
                         tc_commit(bar_pvdone);
                         tc_commit(bar_empty(st));
                     }

@@ -91,7 +91,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Longest sleep (ns) a waiting thread asks for between polls of an mbarrier.
 #ifndef SVP_WAIT_SLEEP_NS
-#define SVP_WAIT_SLEEP_NS 0
+#define SVP_WAIT_SLEEP_NS 20000
 #endif
 
 // Bounded wait for the phase with the given parity to complete.  Returns false when

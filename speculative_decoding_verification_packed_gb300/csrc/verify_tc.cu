@@ -34,7 +34,7 @@
 namespace svp {
 
 constexpr int kVK = 128;            // keys per KV tile
-constexpr int kVThreads = 192;
+constexpr int kVThreads = 224;   // producer, S issuer, 4 softmax warps, PV issuer
 constexpr int kSlotBytes = 32768;   // [128 keys][128 d] bf16 = 2 x [128][64] SW128
 constexpr int kSubBytes = 16384;    // [128 keys][64 d]
 constexpr float kSlack = 32.0f;     // P <= 2^32 (exact in bf16 / fp32 accumulation)
@@ -61,6 +61,7 @@ struct VtRows {
     int32_t warp_sums[8];
     int32_t req_off[kReqCache];
     int32_t req_len[kReqCache];
+    int32_t req_ctx[kReqCache];   // contiguous context: first token row (< 2^31, host-checked)
     int32_t pslot[256];   // merge: partial slot of each piece (pieces <= CTAs <= 256)
     int32_t npend;        // merges this CTA owes (it delivered the last piece of a pair)
     int32_t pend[2][8];   // pair, cf, cl, nact, out_row0, hg, u_pair0 (lo, hi)
@@ -76,6 +77,11 @@ __device__ __forceinline__ int32_t rs_req_len(const VtRows *rs, const TcParams &
     if (i < kReqCache)
         return rs->req_len[i];
     return p.ctx_len ? __ldg(p.ctx_len + i) : 0;
+}
+
+__device__ __forceinline__ int32_t rs_req_ctx(const VtRows *rs, const TcParams &p, int32_t i)
+{
+    return i < kReqCache ? rs->req_ctx[i] : (int32_t)__ldg(p.cu_ctx + i);
 }
 
 __device__ __forceinline__ int64_t vt_cta_start(int64_t total, int32_t c, int32_t C)
@@ -148,11 +154,11 @@ __device__ __forceinline__ void vt_seg(const TcParams &p, const VtRows *rs, cons
         ++lo;
     const int32_t q = lo;
     const int32_t per = (prefix[q + 1] - prefix[q]) / p.HG;
-    const int64_t local = u - prefix[q];
+    const int32_t local = (int32_t)(u - prefix[q]);   // < per * HG: fits 32 bits
     s.i = q / p.RB;
-    s.rb = q % p.RB;
-    s.hg = (int32_t)(local / per);
-    s.t0 = (int32_t)(local % per);
+    s.rb = q - s.i * p.RB;
+    s.hg = local / per;
+    s.t0 = local - s.hg * per;
     s.n_tiles = per;
     s.u_pair0 = prefix[q] + (int64_t)s.hg * per;
     const int64_t seg_end = min(ue, s.u_pair0 + per);
@@ -246,6 +252,22 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// A position in the TMA ring: slot index and the parity of that slot's current use.
+// Tracked incrementally so that no role divides by the (runtime) slot count on its loop.
+struct RingPos {
+    uint32_t slot, phase;
+};
+
+__device__ __forceinline__ RingPos ring_add(RingPos r, uint32_t n, uint32_t nslot)
+{
+    r.slot += n;
+    while (r.slot >= nslot) {
+        r.slot -= nslot;
+        r.phase ^= 1u;
+    }
+    return r;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_constant__ TcParams p)
 {
@@ -271,6 +293,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
     const uint32_t bar_ofree = bar0 + 8u * 26, bar_drain = bar0 + 8u * 27;
     const uint32_t bar_merge = bar0 + 8u * 28;
     const int nP = p.nP;                                          // P buffers (1 or 2)
+    auto pbuf = [&](uint32_t x) -> int { return nP == 2 ? (int)(x & 1u) : 0; };
+    auto ppar = [&](uint32_t x) -> uint32_t { return (nP == 2 ? (x >> 1) : x) & 1u; };
     const uint32_t PBYTES = (uint32_t)((NR + 63) / 64) * 16384u;
 
     VtRows *rs = reinterpret_cast<VtRows *>(smem + p.off_misc);
@@ -296,7 +320,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             mbar_init(bar_pvdone(b), 1);
         }
         mbar_init(bar_ofree, 4);
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, 2);   // one commit from each MMA issuer
         mbar_init(bar_merge, 1);
         mbar_fence_init();
         rs->abort_flag = 0;
@@ -340,6 +364,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             if (q % p.RB == 0 && i < kReqCache) {
                 rs->req_off[i] = __ldg(p.cu_slots + i);
                 rs->req_len[i] = p.ctx_len ? __ldg(p.ctx_len + i) : 0;
+                rs->req_ctx[i] = (!p.paged && p.cu_ctx && p.total_tokens > 0) ? (int32_t)__ldg(p.cu_ctx + i) : 0;
             }
         }
         int32_t incl = units;
@@ -390,6 +415,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         // The whole warp runs the loop; lane 0 issues TMA.  For paged context the lanes
         // fetch a tile's page ids in parallel (shared by its K and V), one tile ahead.
         uint32_t it = 0, nseg = 0, seq = 0;
+        RingPos wp = {0u, 0u};
         bool ok = true;
         const uint64_t pol_stream = l2_policy_evict_first();   // each KV byte is read once
         for (int64_t u = cta_s; u < cta_e && ok;) {
@@ -400,22 +426,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             const int32_t g = (s.hg * p.HP) / p.G;
             const int32_t npages = (L + 15) / 16;
             const int32_t *bt_row = p.paged ? p.block_table + (int64_t)s.i * p.max_pages : nullptr;
-            if (nseg > 0) {
-                // lane 0 waits, the warp follows (keeps `ok` warp-uniform)
-                int w_ok = 1;
-                if (lane == 0)
-                    w_ok = mbar_wait(bar_qempty, (nseg - 1) & 1, abort_flag);
-                if (!(ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0))
-                    break;
-            }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar_qfull, (uint32_t)((D / 64) * 64 * p.HP * p.R * 2));
-                for (int dc = 0; dc < D / 64; ++dc)
-                    tma_load_3d(sbase + p.off_q + dc * QSUB, &p.tm_q, bar_qfull, dc * 64,
-                                s.hg * p.HP, off + s.rb * p.R);
-            }
             ++nseg;
-            const int64_t cctx = (!p.paged && L > 0) ? __ldg(p.cu_ctx + s.i) : 0;
+            const int32_t cctx = (!p.paged && L > 0) ? rs_req_ctx(rs, p, s.i) : 0;
             // page id of lane pp (< 8) for context tile t
             auto page_id = [&](int32_t t) -> int32_t {
                 const int32_t pg = t * (kVK / 16) + lane;
@@ -439,10 +451,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     const CUtensorMap *mc = kv ? &p.tm_vc : &p.tm_kc;
                     const CUtensorMap *mn = kv ? &p.tm_vn : &p.tm_kn;
                     for (int h = 0; h < DH; ++h, ++seq) {
-                        const int sl = seq % nslot;
+                        const int sl = (int)wp.slot;
                         int w_ok = 1;
                         if (lane == 0)
-                            w_ok = mbar_wait(bar_empty(sl), ((seq / nslot) & 1) ^ 1, abort_flag);
+                            w_ok = mbar_wait(bar_empty(sl), wp.phase ^ 1u, abort_flag);
+                        wp = ring_add(wp, 1u, (uint32_t)nslot);
                         if (!(ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0))
                             break;
                         const uint32_t dst = sbase + p.off_ring + sl * kSlotBytes;
@@ -458,7 +471,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                         } else if (lane == 0) {
                             if (t < s.n_ctx) {
                                 mbar_arrive_expect_tx(bar_full(sl), (uint32_t)kSlotBytes);
-                                const int32_t row = (int32_t)(cctx + (int64_t)t * kVK);
+                                const int32_t row = cctx + t * kVK;
                                 for (int c = 0; c < 2; ++c)
                                     tma_load_3d_hint(dst + c * kSubBytes, mc, bar_full(sl),
                                                      h * 128 + c * 64, g, row, pol_stream);
@@ -481,13 +494,86 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             const uint32_t first = seq > (uint32_t)nslot ? seq - nslot : 0;
             for (uint32_t k = first; k < seq; ++k)
                 mbar_wait(bar_full(k % nslot), (k / nslot) & 1, &drain_abort);
-            if (nseg > 0)
-                mbar_wait(bar_qfull, (nseg - 1) & 1, &drain_abort);
         }
     } else if (warp == 1) {
-        // ================================================================ MMA issuer
+        // ================================================================ S^T issuer
+        // S^T = K Q^T of each tile into S buffer it & 1.  The tensor pipe accepts one MMA at
+        // a time and a thread's later shared-memory operations queue behind its MMAs, so S
+        // and PV are issued by two warps: each one blocks only on its own inputs and the
+        // pipe always has the other's work queued.
         if (lane == 0) {
             uint32_t it = 0, nseg = 0;
+            RingPos kpos = {0u, 0u};                     // ring position of K(it)
+            bool ok = true;
+            for (int64_t u = cta_s; u < cta_e && ok;) {
+                VtSeg s;
+                vt_seg(p, rs, prefix, NQ, u, cta_e, cta_s, s);
+                const int32_t off = rs_req_off(rs, p, s.i);
+                const int32_t k_i = (s.i + 1 < kReqCache && s.i + 1 < p.n ? rs->req_off[s.i + 1]
+                                                                          : __ldg(p.cu_slots + s.i + 1)) - off;
+                const int32_t kk = min(k_i - s.rb * p.R, p.R);
+                const uint32_t NRs = (uint32_t)((p.HP * kk + 31) / 32 * 32);
+                const uint32_t idesc_s = idesc_bf16_f32(128, NRs, false, false);
+                const uint32_t qsub16 = QSUB >> 4;
+                // Q of this segment replaces the previous one once its last S^T is done;
+                // the KV stream of this segment is already under way meanwhile
+                if (nseg > 0 && !(ok = mbar_wait(bar_qempty, (nseg - 1) & 1, abort_flag)))
+                    break;
+                mbar_arrive_expect_tx(bar_qfull, (uint32_t)((D / 64) * 64 * p.HP * p.R * 2));
+                for (int dc = 0; dc < D / 64; ++dc)
+                    tma_load_3d(sbase + p.off_q + dc * QSUB, &p.tm_q, bar_qfull, dc * 64,
+                                s.hg * p.HP, off + s.rb * p.R);
+                if (!(ok = mbar_wait(bar_qfull, nseg & 1, abort_flag))) {
+                    volatile int drain_abort = 0;   // the Q copy lands before the CTA exits
+                    mbar_wait(bar_qfull, nseg & 1, &drain_abort);
+                    break;
+                }
+                const int32_t nt = s.t1 - s.t0;
+                for (int32_t k = 0; k < nt; ++k, ++it) {
+                    const int b = it & 1;
+                    if (!(ok = mbar_wait(bar_sfree(b), ((it >> 1) & 1) ^ 1, abort_flag)))
+                        break;
+                    for (int h = 0; h < DH && ok; ++h) {
+                        const RingPos q = ring_add(kpos, (uint32_t)h, (uint32_t)nslot);
+                        ok = mbar_wait(bar_full(q.slot), q.phase, abort_flag);
+                    }
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    // descriptors formed up front, MMAs back to back (a 16-byte step in
+                    // shared memory is +1 in a descriptor's address field)
+                    for (int h = 0; h < DH; ++h) {
+                        const uint64_t ad = sw128_desc(
+                            sbase + p.off_ring + ring_add(kpos, (uint32_t)h, (uint32_t)nslot).slot * kSlotBytes,
+                            16, 1024);
+                        const uint64_t bd = sw128_desc(sbase + p.off_q + 2 * h * QSUB, 16, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc_mma_ss(tmem + TM_S + b * NR,
+                                      ad + (uint64_t)((ks >> 2) * (kSubBytes >> 4) + (ks & 3) * 2),
+                                      bd + (uint64_t)((ks >> 2) * qsub16 + (ks & 3) * 2), idesc_s,
+                                      (h | ks) ? 1u : 0u);
+                    }
+                    tc_commit(bar_sfull(b));
+                    for (int h = 0; h < DH; ++h)
+                        tc_commit(bar_empty(ring_add(kpos, (uint32_t)h, (uint32_t)nslot).slot));
+                    if (k == nt - 1)
+                        tc_commit(bar_qempty);   // Q no longer read by this segment
+                    kpos = ring_add(kpos, 2u * DH, (uint32_t)nslot);
+                }
+                ++nseg;
+                u += nt;
+            }
+            tc_commit(bar_drain);
+            volatile int drain_abort = 0;
+            mbar_wait(bar_drain, 0, &drain_abort);
+        }
+    } else if (warp == 6) {
+        // ================================================================ PV issuer
+        // O^T += V^T P^T and l^T += 1 P^T of each tile, from P buffer pbuf(it).
+        if (lane == 0) {
+            uint32_t it = 0, nseg = 0;
+            RingPos ppos = {0u, 0u};                     // ring position of K(it)
             bool ok = true;
             for (int64_t u = cta_s; u < cta_e && ok;) {
                 VtSeg s;
@@ -498,102 +584,47 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 const int32_t L = rs_req_len(rs, p, s.i);
                 const int32_t kk = min(k_i - s.rb * p.R, p.R);
                 const uint32_t NRs = (uint32_t)((p.HP * kk + 31) / 32 * 32);
-                const uint32_t idesc_s = idesc_bf16_f32(128, NRs, false, false);
                 const uint32_t idesc_o = idesc_bf16_f32(128, NRs, true, true);
                 const uint32_t idesc_l = idesc_bf16_f32(128, NRs, false, true);
-                if (!(ok = mbar_wait(bar_qfull, nseg & 1, abort_flag)))
-                    break;
-                tc_fence_after();
+                const uint64_t ao = sw128_desc(sbase + p.off_ones, 16, 0);
                 const int32_t nt = s.t1 - s.t0;
-                // Issue S^T of tile kS and PV of tile kP as soon as each is ready (polling),
-                // so a PV never waits behind the next tile's K load.  S runs at most two
-                // tiles ahead (two S buffers).
-                int32_t kS = 0, kP = 0;
-                bool ofree_ok = (nseg == 0);
-                uint32_t idle = 0;
-                uint64_t idle_t0 = 0;
-                while (kP < nt) {
-                    bool did = false;
-                    if (kS < nt && kS < kP + 2) {
-                        const uint32_t itk = it + kS;
-                        const int b = itk & 1;
-                        bool ready = mbar_test_wait(bar_sfree(b), ((itk >> 1) & 1) ^ 1);
-                        for (int h = 0; h < DH && ready; ++h) {
-                            const uint32_t sq = itk * 2 * DH + h;
-                            ready = mbar_test_wait(bar_full(sq % nslot), (sq / nslot) & 1);
-                        }
-                        if (ready) {
-                            tc_fence_after();
-                            for (int h = 0; h < DH; ++h) {
-                                const uint32_t ka = sbase + p.off_ring + ((itk * 2 * DH + h) % nslot) * kSlotBytes;
-                                for (int ks = 0; ks < 8; ++ks) {
-                                    const uint32_t a = ka + (ks >> 2) * kSubBytes + (ks & 3) * 32;
-                                    const uint32_t bq = sbase + p.off_q + (2 * h + (ks >> 2)) * QSUB + (ks & 3) * 32;
-                                    tc_mma_ss(tmem + TM_S + b * NR, sw128_desc(a, 16, 1024),
-                                              sw128_desc(bq, 16, 1024), idesc_s, (h | ks) ? 1u : 0u);
-                                }
-                            }
-                            tc_commit(bar_sfull(b));
-                            for (int h = 0; h < DH; ++h)
-                                tc_commit(bar_empty((itk * 2 * DH + h) % nslot));
-                            if (kS == nt - 1)
-                                tc_commit(bar_qempty);   // Q no longer read by this segment
-                            ++kS;
-                            did = true;
-                        }
-                    }
-                    if (kP < kS) {
-                        const uint32_t itp = it + kP;
-                        const int pb = (int)(itp % (uint32_t)nP);
-                        if (!ofree_ok)
-                            ofree_ok = mbar_test_wait(bar_ofree, (nseg - 1) & 1);
-                        bool ready = (kP > 0 || ofree_ok) &&
-                                     mbar_test_wait(bar_pfull(pb), (itp / nP) & 1);
-                        for (int h = 0; h < DH && ready; ++h) {
-                            const uint32_t sq = itp * 2 * DH + DH + h;
-                            ready = mbar_test_wait(bar_full(sq % nslot), (sq / nslot) & 1);
-                        }
-                        if (ready) {
-                            tc_fence_after();
-                            const int32_t t = s.t0 + kP;
-                            const int32_t kv = vt_kvalid(p, s, t, L, k_i);
-                            const int32_t k16 = (kv + 15) / 16;
-                            const uint32_t pbase = sbase + p.off_p + pb * PBYTES;
-                            for (int h = 0; h < DH; ++h) {
-                                const uint32_t va = sbase + p.off_ring + ((itp * 2 * DH + DH + h) % nslot) * kSlotBytes;
-                                for (int ks = 0; ks < k16; ++ks)
-                                    tc_mma_ss(tmem + TM_O + h * NR, sw128_desc(va + ks * 2048, kSubBytes, 1024),
-                                              sw128_desc(pbase + ks * 2048, 16384, 1024), idesc_o,
-                                              (kP == 0 && ks == 0) ? 0u : 1u);
-                            }
-                            for (int ks = 0; ks < k16; ++ks)
-                                tc_mma_ss(tmem + TM_L, sw128_desc(sbase + p.off_ones, 16, 0),
-                                          sw128_desc(pbase + ks * 2048, 16384, 1024), idesc_l,
-                                          (kP == 0 && ks == 0) ? 0u : 1u);
-                            tc_commit(bar_pvdone(pb));
-                            for (int h = 0; h < DH; ++h)
-                                tc_commit(bar_empty((itp * 2 * DH + DH + h) % nslot));
-                            ++kP;
-                            did = true;
-                        }
-                    }
-                    if (did) {
-                        idle = 0;
-                    } else {
-                        if (idle++ == 0)
-                            idle_t0 = global_ns();
-                        if ((idle & 255u) == 0) {
-                            if (*abort_flag || global_ns() - idle_t0 > kWaitLimitNs) {
-                                *abort_flag = 1;
-                                ok = false;
-                                break;
-                            }
-                        }
-                    }
-                }
-                if (!ok)
+                // O^T of this segment may be written once the previous epilogue read it
+                if (nseg > 0 && !(ok = mbar_wait(bar_ofree, (nseg - 1) & 1, abort_flag)))
                     break;
-                it += nt;
+                for (int32_t k = 0; k < nt; ++k, ++it) {
+                    const int pb = pbuf(it);
+                    if (!(ok = mbar_wait(bar_pfull(pb), ppar(it), abort_flag)))
+                        break;
+                    for (int h = 0; h < DH && ok; ++h) {
+                        const RingPos q = ring_add(ppos, (uint32_t)(DH + h), (uint32_t)nslot);
+                        ok = mbar_wait(bar_full(q.slot), q.phase, abort_flag);
+                    }
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const int32_t kv = vt_kvalid(p, s, s.t0 + k, L, k_i);
+                    const int32_t k16 = (kv + 15) / 16;
+                    const uint64_t bp = sw128_desc(sbase + p.off_p + pb * PBYTES, 16384, 1024);
+                    const uint32_t acc0 = k == 0 ? 0u : 1u;
+                    for (int h = 0; h < DH; ++h) {
+                        const uint64_t av = sw128_desc(
+                            sbase + p.off_ring + ring_add(ppos, (uint32_t)(DH + h), (uint32_t)nslot).slot * kSlotBytes,
+                            kSubBytes, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            if (ks < k16)   // 16 keys (2048 bytes) per MMA
+                                tc_mma_ss(tmem + TM_O + h * NR, av + (uint64_t)(ks * 128),
+                                          bp + (uint64_t)(ks * 128), idesc_o, ks ? 1u : acc0);
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        if (ks < k16)
+                            tc_mma_ss(tmem + TM_L, ao, bp + (uint64_t)(ks * 128), idesc_l, ks ? 1u : acc0);
+                    tc_commit(bar_pvdone(pb));
+                    for (int h = 0; h < DH; ++h)
+                        tc_commit(bar_empty(ring_add(ppos, (uint32_t)(DH + h), (uint32_t)nslot).slot));
+                    ppos = ring_add(ppos, 2u * DH, (uint32_t)nslot);
+                }
                 ++nseg;
                 u += nt;
             }
@@ -640,7 +671,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     break;
                 tc_fence_after();
                 const uint32_t sa = tmem + lane_off + TM_S + b * NR;
-                const uint32_t pline = sbase + p.off_p + (it % (uint32_t)nP) * PBYTES + t * 128;
+                const uint32_t pline = sbase + p.off_p + pbuf(it) * PBYTES + t * 128;
                 const uint32_t mref_a = smem_u32(rs->m_ref), jr_a = smem_u32(rs->jr);
                 if (k == 0) {
                     // seed the reference of every live row with the score of key 0 of
@@ -681,7 +712,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 const bool hit = ymax > kSlack;
                 // this P buffer is read by PV of tile it - nP
                 if (it >= (uint32_t)nP &&
-                    !(ok = mbar_wait(bar_pvdone(it % nP), ((it - nP) / nP) & 1, abort_flag)))
+                    !(ok = mbar_wait(bar_pvdone(pbuf(it)), ppar(it - nP), abort_flag)))
                     break;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -736,7 +767,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     if (rs->rescale) {
                         // O^T halves and l^T: column r scaled by alpha[r], once PV of the
                         // previous tile is complete
-                        if (!(ok = mbar_wait(bar_pvdone((it - 1) % nP), ((it - 1) / nP) & 1, abort_flag)))
+                        if (!(ok = mbar_wait(bar_pvdone(pbuf(it - 1)), ppar(it - 1), abort_flag)))
                             break;
                         tc_fence_after();
                         for (int m = 0; m <= DH; ++m) {
@@ -796,14 +827,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar_pfull(it % nP));
+                    mbar_arrive(bar_pfull(pbuf(it)));
                 if (!ok)
                     break;
             }
             if (!ok)
                 break;
             // ---- epilogue: O^T, l^T complete after the last PV of the segment
-            if (!(ok = mbar_wait(bar_pvdone((it - 1) % nP), ((it - 1) / nP) & 1, abort_flag)))
+            if (!(ok = mbar_wait(bar_pvdone(pbuf(it - 1)), ppar(it - 1), abort_flag)))
                 break;
             tc_fence_after();
             // row sums: every lane of l^T holds l for each column
@@ -882,8 +913,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 }
                 named_bar_sync(1, 128);
                 if (rs->last && stid == 0) {
-                    // this CTA delivered the pair's last piece: merge it after its range,
-                    // when the TMA ring is idle
                     int32_t *e = rs->pend[rs->npend++];
                     e[0] = s.pair; e[1] = cf; e[2] = cl; e[3] = nact; e[4] = out_row0; e[5] = s.hg;
                     e[6] = (int32_t)(s.u_pair0 & 0xffffffff); e[7] = (int32_t)(s.u_pair0 >> 32);
@@ -893,8 +922,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             ++nseg;
             u += nt;
         }
-        // ---- merges owed by this CTA: partial slabs -> TMA ring (one bulk copy per
-        // piece), then weights x slabs from shared memory; pieces in order.
+        // ---- merges owed by this CTA (it delivered the pair's last piece): partial slabs
+        // -> TMA ring (one bulk copy per piece), then weights x slabs from shared memory;
+        // pieces in order.
         named_bar_sync(1, 128);
         const int npend = ok ? rs->npend : 0;
         uint32_t merge_phase = 0;
