@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
     auto bar_pvdone = [&](int b) { return bar0 + 8u * (24 + b); };   // per P buffer
     const uint32_t bar_ofree = bar0 + 8u * 26, bar_drain = bar0 + 8u * 27;
     const uint32_t bar_merge = bar0 + 8u * 28;
+    const uint32_t bar_tick = bar0 + 8u * 29;   // merges owed by this CTA are known
     const int nP = p.nP;                                          // P buffers (1 or 2)
     auto pbuf = [&](uint32_t x) -> int { return nP == 2 ? (int)(x & 1u) : 0; };
     auto ppar = [&](uint32_t x) -> uint32_t { return (nP == 2 ? (x >> 1) : x) & 1u; };
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         mbar_init(bar_ofree, 4);
         mbar_init(bar_drain, 2);   // one commit from each MMA issuer
         mbar_init(bar_merge, 1);
+        mbar_init(bar_tick, 1);
         mbar_fence_init();
         rs->abort_flag = 0;
         rs->flag[0] = rs->flag[1] = 0;
@@ -575,6 +577,29 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             uint32_t it = 0, nseg = 0;
             RingPos ppos = {0u, 0u};                     // ring position of K(it)
             bool ok = true;
+            // A segment that holds part of a (request, row block, head group) pair leaves
+            // a partial result; its pair ticket is taken here, while this warp waits for
+            // the epilogue anyway.  The partial stores precede the epilogue's arrive on
+            // ofree (release), this thread's wait acquires them, and the gpu-scope fence
+            // below is cumulative over them.  The ticket values are read at the end only.
+            VtSeg sp = {};
+            int32_t sp_nact = 0, sp_row0 = 0;
+            int32_t ntk = 0, tk0 = 0, tk1 = 0;
+            VtSeg tks0 = {}, tks1 = {};
+            int32_t tkn0 = 0, tkr0 = 0, tkn1 = 0, tkr1 = 0;
+            auto take_ticket = [&]() {
+                if (sp.single)
+                    return;
+                __threadfence();
+                if (ntk == 0) {
+                    tk0 = atomicAdd(p.tickets + sp.pair, 1);
+                    tks0 = sp; tkn0 = sp_nact; tkr0 = sp_row0;
+                } else {
+                    tk1 = atomicAdd(p.tickets + sp.pair, 1);
+                    tks1 = sp; tkn1 = sp_nact; tkr1 = sp_row0;
+                }
+                ++ntk;
+            };
             for (int64_t u = cta_s; u < cta_e && ok;) {
                 VtSeg s;
                 vt_seg(p, rs, prefix, NQ, u, cta_e, cta_s, s);
@@ -589,8 +614,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 const uint64_t ao = sw128_desc(sbase + p.off_ones, 16, 0);
                 const int32_t nt = s.t1 - s.t0;
                 // O^T of this segment may be written once the previous epilogue read it
-                if (nseg > 0 && !(ok = mbar_wait(bar_ofree, (nseg - 1) & 1, abort_flag)))
-                    break;
+                if (nseg > 0) {
+                    if (!(ok = mbar_wait(bar_ofree, (nseg - 1) & 1, abort_flag)))
+                        break;
+                    take_ticket();
+                }
+                sp = s;
+                sp_nact = p.HP * kk;
+                sp_row0 = off + s.rb * p.R;
                 for (int32_t k = 0; k < nt; ++k, ++it) {
                     const int pb = pbuf(it);
                     if (!(ok = mbar_wait(bar_pfull(pb), ppar(it), abort_flag)))
@@ -628,6 +659,27 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 ++nseg;
                 u += nt;
             }
+            if (ok && nseg > 0 && (ok = mbar_wait(bar_ofree, (nseg - 1) & 1, abort_flag)))
+                take_ticket();
+            if (ok) {
+                // the pair's last arrival merges it after this CTA's range
+                int32_t npend = 0;
+                for (int q = 0; q < ntk; ++q) {
+                    const VtSeg &e = q ? tks1 : tks0;
+                    const int32_t cf = vt_cta_of_unit(e.u_pair0, total, ncta);
+                    const int32_t cl = vt_cta_of_unit(e.u_pair0 + e.n_tiles - 1, total, ncta);
+                    if ((q ? tk1 : tk0) == cl - cf) {
+                        int32_t *d = rs->pend[npend++];
+                        d[0] = e.pair; d[1] = cf; d[2] = cl; d[3] = q ? tkn1 : tkn0;
+                        d[4] = q ? tkr1 : tkr0; d[5] = e.hg;
+                        d[6] = (int32_t)(e.u_pair0 & 0xffffffff); d[7] = (int32_t)(e.u_pair0 >> 32);
+                    }
+                }
+                rs->npend = npend;
+                if (npend)
+                    __threadfence();   // acquire side: the other pieces' partials are visible
+            }
+            mbar_arrive(bar_tick);
             tc_commit(bar_drain);
             volatile int drain_abort = 0;
             mbar_wait(bar_drain, 0, &drain_abort);
@@ -899,24 +951,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 if (stid < nact)
                     st_global_f2_hint(p.part_ml + (int64_t)slot * kRows + stid,
                                       make_float2(rs->m_ref[stid], rs->lrow[stid]), pol_keep);
+                // the partial stores of this warp precede its arrive (the PV issuer takes
+                // the pair's ticket after it)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(bar_ofree);
-                __threadfence();
-                named_bar_sync(1, 128);
-                const int32_t cf = vt_cta_of_unit(s.u_pair0, total, ncta);
-                const int32_t cl = vt_cta_of_unit(s.u_pair0 + s.n_tiles - 1, total, ncta);
-                if (stid == 0) {
-                    const int prev = atomicAdd(p.tickets + s.pair, 1);
-                    rs->last = (prev == cl - cf) ? 1 : 0;
-                }
-                named_bar_sync(1, 128);
-                if (rs->last && stid == 0) {
-                    int32_t *e = rs->pend[rs->npend++];
-                    e[0] = s.pair; e[1] = cf; e[2] = cl; e[3] = nact; e[4] = out_row0; e[5] = s.hg;
-                    e[6] = (int32_t)(s.u_pair0 & 0xffffffff); e[7] = (int32_t)(s.u_pair0 >> 32);
-                }
             }
             named_bar_sync(1, 128);
             ++nseg;
@@ -925,7 +965,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         // ---- merges owed by this CTA (it delivered the pair's last piece): partial slabs
         // -> TMA ring (one bulk copy per piece), then weights x slabs from shared memory;
         // pieces in order.
-        named_bar_sync(1, 128);
+        if (ok)
+            ok = mbar_wait(bar_tick, 0, abort_flag);
         const int npend = ok ? rs->npend : 0;
         uint32_t merge_phase = 0;
         for (int pi = 0; pi < npend && ok; ++pi) {
@@ -943,7 +984,23 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 rs->orow[r] = ((int64_t)(out_row0 + r / p.HP) * p.hq + hg * p.HP + r % p.HP) * D;
             }
             named_bar_sync(1, 128);
-            // per row: merged max M and sum L over the pieces, one online pass
+            const uint32_t slab = (uint32_t)(((int64_t)nact * D * 4 + 127) / 128 * 128);
+            const int32_t cap_ring = (int32_t)((uint32_t)(nslot * kSlotBytes) / slab);
+            const int32_t cap = cap_ring < 8 ? cap_ring : 8;
+            // the first pass's slabs are on their way while the row statistics are formed
+            auto issue_pass = [&](int32_t c0) {
+                const int32_t nb = min(cap, np - c0);
+                asm volatile("fence.proxy.async;" ::: "memory");
+                mbar_arrive_expect_tx(bar_merge, (uint32_t)nb * slab);
+                for (int q = 0; q < nb; ++q)
+                    bulk_g2s(sbase + p.off_ring + q * slab,
+                             p.part_o + (int64_t)rs->pslot[c0 + q] * kRows * D, slab, bar_merge);
+            };
+            if (stid == 0)
+                issue_pass(0);
+            // per row: merged max M and sum L over the pieces, one online pass; with at
+            // most 8 pieces the weights 2^(m_q - M) come out of the same pass
+            const bool one_block = np <= 8;
             if (stid < nact) {
                 const int r = stid;
                 float M = -INFINITY, Ls = 0.0f;
@@ -964,30 +1021,31 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                             Lb += ml[q].y * fast_exp2(ml[q].x - Mb);
                     M = Mb;
                     Ls = Lb;
+                    if (one_block) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if (q < np)
+                                rs->wts[q][r] = fast_exp2(ml[q].x - M);
+                    }
                 }
                 rs->m_ref[r] = M;
                 rs->linv[r] = 1.0f / Ls;
                 if (p.lse)
                     p.lse[rs->orow[r] / D] = (M + __log2f(Ls)) * 0.69314718055994531f;
             }
-            const uint32_t slab = (uint32_t)(((int64_t)nact * D * 4 + 127) / 128 * 128);
-            const int32_t cap_ring = (int32_t)((uint32_t)(nslot * kSlotBytes) / slab);
-            const int32_t cap = cap_ring < 8 ? cap_ring : 8;
             constexpr int C4 = D / 4;
             constexpr int RGS = 128 / C4;
             const int col4 = stid % C4, rg = stid / C4;
             const int32_t slot0 = rs->pslot[0];
             for (int32_t c0 = 0; c0 < np && ok; c0 += cap) {
                 const int32_t nb = min(cap, np - c0);
-                named_bar_sync(1, 128);
-                if (stid == 0) {
-                    asm volatile("fence.proxy.async;" ::: "memory");
-                    mbar_arrive_expect_tx(bar_merge, (uint32_t)nb * slab);
-                    for (int q = 0; q < nb; ++q)
-                        bulk_g2s(sbase + p.off_ring + q * slab,
-                                 p.part_o + (int64_t)rs->pslot[c0 + q] * kRows * D, slab, bar_merge);
+                const int32_t wq0 = one_block ? c0 : 0;   // weights of this pass: wts[wq0 + q]
+                if (c0 > 0) {
+                    named_bar_sync(1, 128);              // the ring was read by the last pass
+                    if (stid == 0)
+                        issue_pass(c0);
                 }
-                if (stid < nact) {
+                if (!one_block && stid < nact) {
                     const int r = stid;
                     for (int q = 0; q < nb; ++q)
                         rs->wts[q][r] = fast_exp2(__ldcg(p.part_ml + (int64_t)rs->pslot[c0 + q] * kRows + r).x -
@@ -1004,7 +1062,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                         acc = __ldcg(reinterpret_cast<const float4 *>(p.part_o + ((int64_t)slot0 * kRows + r) * D) + col4);
                     for (int q = 0; q < nb; ++q) {
                         const float4 x = ld_shared_f4(sbase + p.off_ring + q * slab + (r * D + col4 * 4) * 4);
-                        const float wq = rs->wts[q][r];
+                        const float wq = rs->wts[wq0 + q][r];
                         acc.x += wq * x.x;
                         acc.y += wq * x.y;
                         acc.z += wq * x.z;
@@ -1082,7 +1140,7 @@ static bool verify_tc_layout_np(int d, int NR, int nP, TcParams &p)
     p.off_q = off; off += q;
     p.off_p = off; off += pt;
     p.off_ones = off; off += 1024;
-    p.off_bar = off; off += 29 * 8;
+    p.off_bar = off; off += 30 * 8;
     off = (off + 15) / 16 * 16;
     p.off_misc = off; off += (int)sizeof(VtRows);
     off = (off + 15) / 16 * 16;
