@@ -13,7 +13,7 @@ namespace svp {
 // ---- kernels defined in the other translation units
 svp_status attn_tc_launch(const TcParams &p, int d, int grid, cudaStream_t stream);
 svp_status verify_tc_launch(const TcParams &p, int d, int grid, cudaStream_t stream);
-bool verify_tc_layout(int d, int NR, TcParams &p);
+bool verify_tc_layout(int d, int NR, int grid, TcParams &p);
 int attn_tc_max_prefix();
 int attn_tc_block_keys();
 svp_status attn_simt_launch(const SimtParams &p, cudaStream_t stream);
@@ -369,7 +369,7 @@ static svp_status verify_impl(const void *q, const void *k_new, const void *v_ne
     p.part_ml = reinterpret_cast<float2 *>(wsb + pl.off_part_ml);
     p.sig = (pl.transposed << 20) | (pl.mode << 12) | d;
     if (pl.transposed) {
-        if (!verify_tc_layout(d, pl.NR, p))
+        if (!verify_tc_layout(d, pl.NR, pl.grid, p))
             return SVP_EUNSUPPORTED;
         return verify_tc_launch(p, d, pl.grid, stream);
     }

@@ -40,6 +40,7 @@ struct TcParams {
     int32_t sig;                 // workspace layout signature (header word 1)
     // transposed short-tile kernel only: tile rows and shared-memory layout
     int32_t NR, nslot, tmem_cols, smem_bytes, nP;
+    int32_t cost0;               // partition cost of starting a pair, in KV tiles
     int32_t off_q, off_p, off_ones, off_ring, off_bar, off_misc, off_pref;
 };
 

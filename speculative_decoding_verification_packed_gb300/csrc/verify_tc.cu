@@ -41,6 +41,7 @@ constexpr float kSlack = 32.0f;     // P <= 2^32 (exact in bf16 / fp32 accumulat
 
 // Shared per-row softmax state (in the misc region).
 constexpr int kReqCache = 256;      // requests whose (offset, context length) sit in smem
+constexpr int kPairCost = 4;        // partition cost of starting a pair (segment switch + merge), in tiles
 
 struct VtRows {
     float m_ref[128];
@@ -59,6 +60,7 @@ struct VtRows {
     int32_t abort_flag;
     uint32_t tmem;
     int32_t warp_sums[8];
+    int32_t warp_costs[8];
     int32_t req_off[kReqCache];
     int32_t req_len[kReqCache];
     int32_t req_ctx[kReqCache];   // contiguous context: first token row (< 2^31, host-checked)
@@ -84,14 +86,49 @@ __device__ __forceinline__ int32_t rs_req_ctx(const VtRows *rs, const TcParams &
     return i < kReqCache ? rs->req_ctx[i] : (int32_t)__ldg(p.cu_ctx + i);
 }
 
-__device__ __forceinline__ int64_t vt_cta_start(int64_t total, int32_t c, int32_t C)
+// The CTAs split the KV tiles of all (request, row block, head group) pairs in order, in
+// equal shares of a cost that charges every pair cost0 tiles at its start: the CTA that
+// starts a pair also pays the segment switch into it and, as a rule, the pair's merge.
+// prefix[q] / cprefix[q]: tiles / cost before (request, row block) q (each of its HG pairs
+// has nt tiles and costs nt + cost0, or nothing when nt = 0).
+// First tile at or after cost unit v (v <= ctot).
+__device__ __forceinline__ int32_t vt_tile_of_cost(const int32_t *prefix, const int32_t *cprefix,
+                                                   int32_t nq, int32_t hg_n, int32_t cost0,
+                                                   int32_t v)
 {
-    return (int64_t)c * total / C;
+    if (v >= cprefix[nq])
+        return prefix[nq];
+    int32_t lo = 0, hi = nq;
+    while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (cprefix[mid] <= v)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    while (cprefix[lo + 1] <= v)
+        ++lo;
+    const int32_t pc = (cprefix[lo + 1] - cprefix[lo]) / hg_n;   // nt + cost0
+    const int32_t nt = pc - cost0;
+    const int32_t lc = v - cprefix[lo];
+    const int32_t hg = lc / pc;
+    const int32_t loc = lc - hg * pc;
+    return prefix[lo] + hg * nt + (loc > cost0 ? loc - cost0 : 0);
 }
 
-__device__ __forceinline__ int32_t vt_cta_of_unit(int64_t u, int64_t total, int32_t C)
+// CTA c owns tiles [ctile[c], ctile[c+1]); the owner of tile u is the last c with
+// ctile[c] <= u (CTAs with an empty range never own a tile inside a pair).
+__device__ __forceinline__ int32_t vt_cta_of_unit(const int32_t *ctile, int32_t ncta, int64_t u)
 {
-    return (int32_t)(((u + 1) * C + total - 1) / total - 1);
+    int32_t lo = 0, hi = ncta;   // ctile[lo] <= u < ctile[hi]
+    while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (ctile[mid] <= u)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
 }
 
 struct VtSeg {
@@ -300,8 +337,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
 
     VtRows *rs = reinterpret_cast<VtRows *>(smem + p.off_misc);
     volatile int *abort_flag = &rs->abort_flag;
-    int32_t *prefix = reinterpret_cast<int32_t *>(smem + p.off_pref);
     const int32_t NQ = p.n * p.RB;
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + p.off_pref);   // [NQ + 1]
+    int32_t *cprefix = prefix + (NQ + 1);                                 // [NQ + 1]
+    int32_t *ctile = cprefix + (NQ + 1);                                  // [gridDim.x + 1]
     // start the workspace-signature load early; it is checked after the prologue
     const int32_t sig_seen = (tid == 0) ? *reinterpret_cast<volatile int32_t *>(p.status + 1) : 0;
 
@@ -349,19 +388,22 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                      0x3f803f80u);
     fence_proxy_async_smem();
 
-    // prefix sums of KV tiles over (request, row block)
+    // prefix sums of KV tiles and of partition cost over (request, row block)
     int32_t bad_bits = 0;
-    if (tid == 0)
+    if (tid == 0) {
         prefix[0] = 0;
-    int32_t running = 0;
+        cprefix[0] = 0;
+    }
+    int32_t running = 0, crunning = 0;
     for (int32_t base = 0; base < NQ; base += kVThreads) {
         const int32_t q = base + tid;
-        int32_t units = 0;
+        int32_t units = 0, costs = 0;
         if (q < NQ) {
             int32_t nt, bad;
             vt_units(p, q / p.RB, q % p.RB, nt, bad);
             bad_bits |= bad;
             units = nt * p.HG;
+            costs = nt > 0 ? (nt + p.cost0) * p.HG : 0;
             const int32_t i = q / p.RB;
             if (q % p.RB == 0 && i < kReqCache) {
                 rs->req_off[i] = __ldg(p.cu_slots + i);
@@ -369,24 +411,35 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 rs->req_ctx[i] = (!p.paged && p.cu_ctx && p.total_tokens > 0) ? (int32_t)__ldg(p.cu_ctx + i) : 0;
             }
         }
-        int32_t incl = units;
+        int32_t incl = units, cincl = costs;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
+            const int32_t cv = __shfl_up_sync(0xffffffffu, cincl, o);
+            if (lane >= o) {
                 incl += v;
+                cincl += cv;
+            }
         }
         __syncthreads();
-        if (lane == 31)
+        if (lane == 31) {
             rs->warp_sums[warp] = incl;
+            rs->warp_costs[warp] = cincl;
+        }
         __syncthreads();
-        int32_t before = running;
-        for (int w2 = 0; w2 < warp; ++w2)
+        int32_t before = running, cbefore = crunning;
+        for (int w2 = 0; w2 < warp; ++w2) {
             before += rs->warp_sums[w2];
-        if (q < NQ)
+            cbefore += rs->warp_costs[w2];
+        }
+        if (q < NQ) {
             prefix[q + 1] = before + incl;
-        for (int w2 = 0; w2 < kVThreads / 32; ++w2)
+            cprefix[q + 1] = cbefore + cincl;
+        }
+        for (int w2 = 0; w2 < kVThreads / 32; ++w2) {
             running += rs->warp_sums[w2];
+            crunning += rs->warp_costs[w2];
+        }
     }
     if (bad_bits && blockIdx.x == 0)
         set_status(p.status, bad_bits);
@@ -399,16 +452,22 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         if (seen == 0 && blockIdx.x == 0)
             p.status[1] = p.sig;
     }
+    __syncthreads();
+    // tile range of every CTA: equal shares of the partition cost
+    const int64_t total = rs->last ? 0 : prefix[NQ];
+    const int32_t ctot = cprefix[NQ];
+    const int32_t ncta = total > 0 ? (int32_t)((int64_t)gridDim.x < (int64_t)ctot ? gridDim.x : ctot) : 0;
+    for (int32_t c = tid; c <= ncta; c += kVThreads)
+        ctile[c] = vt_tile_of_cost(prefix, cprefix, NQ, p.HG, p.cost0,
+                                   (int32_t)((int64_t)c * ctot / (ncta > 0 ? ncta : 1)));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = rs->tmem;
-    const int64_t total = rs->last ? 0 : prefix[NQ];
-    const int32_t ncta = (int32_t)((int64_t)gridDim.x < total ? (int64_t)gridDim.x : total);
     int64_t cta_s = 0, cta_e = 0;
     if ((int32_t)blockIdx.x < ncta) {
-        cta_s = vt_cta_start(total, blockIdx.x, ncta);
-        cta_e = vt_cta_start(total, blockIdx.x + 1, ncta);
+        cta_s = ctile[blockIdx.x];
+        cta_e = ctile[blockIdx.x + 1];
     }
     const uint32_t TM_S = 0, TM_O = 2u * NR, TM_L = (2u + DH) * NR;
 
@@ -666,8 +725,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 int32_t npend = 0;
                 for (int q = 0; q < ntk; ++q) {
                     const VtSeg &e = q ? tks1 : tks0;
-                    const int32_t cf = vt_cta_of_unit(e.u_pair0, total, ncta);
-                    const int32_t cl = vt_cta_of_unit(e.u_pair0 + e.n_tiles - 1, total, ncta);
+                    const int32_t cf = vt_cta_of_unit(ctile, ncta, e.u_pair0);
+                    const int32_t cl = vt_cta_of_unit(ctile, ncta, e.u_pair0 + e.n_tiles - 1);
                     if ((q ? tk1 : tk0) == cl - cf) {
                         int32_t *d = rs->pend[npend++];
                         d[0] = e.pair; d[1] = cf; d[2] = cl; d[3] = q ? tkn1 : tkn0;
@@ -976,7 +1035,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             const int32_t np = cl - cf + 1;
             for (int32_t q = stid; q < np; q += 128) {
                 const int32_t c = cf + q;
-                const int64_t cs = vt_cta_start(total, c, ncta);
+                const int64_t cs = ctile[c];
                 rs->pslot[q] = 2 * c + ((q == 0 && cs < u_pair0) ? 1 : 0);
             }
             if (stid < nact) {
@@ -1120,17 +1179,18 @@ svp_status verify_tc_launch(const TcParams &p, int d, int grid, cudaStream_t str
 }
 
 // Shared-memory layout of verify_tc_kernel for a tile of NR rows (host helper).
-static bool verify_tc_layout_np(int d, int NR, int nP, TcParams &p);
+static bool verify_tc_layout_np(int d, int NR, int nP, int grid, TcParams &p);
 
-bool verify_tc_layout(int d, int NR, TcParams &p)
+bool verify_tc_layout(int d, int NR, int grid, TcParams &p)
 {
+    p.cost0 = kPairCost;
     // two P buffers when the ring keeps enough slots, else one
-    if (verify_tc_layout_np(d, NR, 2, p) && p.nslot >= (d == 128 ? 5 : 4))
+    if (verify_tc_layout_np(d, NR, 2, grid, p) && p.nslot >= (d == 128 ? 5 : 4))
         return true;
-    return verify_tc_layout_np(d, NR, 1, p);
+    return verify_tc_layout_np(d, NR, 1, grid, p);
 }
 
-static bool verify_tc_layout_np(int d, int NR, int nP, TcParams &p)
+static bool verify_tc_layout_np(int d, int NR, int nP, int grid, TcParams &p)
 {
     const int budget = 227 * 1024;
     const int q = (d / 64) * NR * 128;
@@ -1144,7 +1204,7 @@ static bool verify_tc_layout_np(int d, int NR, int nP, TcParams &p)
     off = (off + 15) / 16 * 16;
     p.off_misc = off; off += (int)sizeof(VtRows);
     off = (off + 15) / 16 * 16;
-    p.off_pref = off; off += (kMaxPrefix + 1) * 4;
+    p.off_pref = off; off += (2 * (p.n * p.RB + 1) + grid + 1) * 4;   // prefix, cprefix, ctile
     off = (off + 1023) / 1024 * 1024;
     p.off_ring = off;
     const int slots = (budget - 1024 - off) / kSlotBytes;
