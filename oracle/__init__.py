@@ -24,6 +24,11 @@ What it computes, with the passages it follows:
   page text, the reading capacity = B*ceil(l/B) is pinned by 112 of 128 rows at l=16,
   B=128 in SII-A).
 
+* ``dvl`` (oracle/dvl.py) -- the DVL budget allocator and flat-buffer packer of
+  Algorithm 1 (DScale SIII-C): prefix scores, initial lengths, grow / shrink to the
+  budget, offsets, row-mapped packing with tail placeholders, and the retention measure
+  of SIV.
+
 Pins (tests/test_oracle_*.py): brute force on tiny inputs, closed forms, the packed vs
 alone / relayout / paged vs contiguous / permutation invariants, numpy argmax and sort
 on planted ties, exhaustive accept patterns, and the worked examples the pages print
