@@ -243,6 +243,44 @@ svp_status svp_margin_accept_noalloc(const void *logits, int64_t row_stride, int
                                      float *top1, float *top2, float *margin,
                                      int32_t *accept_len, int32_t *next_token, void *stream);
 
+/* ---------------------------------------------------------------------------------- */
+/* DVL budget allocator and flat-buffer packer (DScale SIII-C, Budget allocator and     */
+/* Flat-buffer packer, Algorithm 1, Fig. 6), one thread block, no host round trip.       */
+/*   q[i,0] = 1 (anchor); q[i,j] = min(q[i,j-1], scores[i,j-1]) for j = 1..w-1.          */
+/*   k0_i = clip(rint(sum_{j=1}^{w-1} q[i,j]), 1, w) for live requests (the sum in fp32, */
+/*   positions in order; rint = nearest, ties to even), 0 for the others.               */
+/*   budget = budget_per_req * n_live; delta = budget - sum(k0).  delta > 0: the delta   */
+/*   best next slots q[i,k_i] are added (a request grows up to w); delta < 0: the -delta  */
+/*   worst last slots q[i,k_i-1] are removed (never the anchor).  Ties go to the lowest   */
+/*   request index.  This equals the page's one-slot-at-a-time loop because q is         */
+/*   non-increasing along a request.  Growing stops when all live requests reach w,      */
+/*   shrinking when all are at 1.                                                       */
+/*   cu_slots = exclusive prefix sums of k (inactive requests: k = 0, offset = the end). */
+/*   Packed row cu_slots[i] + j of tokens / positions / kv_refs = field[i, j] for j < k_i;*/
+/*   rows cu_slots[n_bs] .. m_cap-1 hold fill_token / fill_pos / fill_ref.               */
+
+/*
+ * scores [n_bs, w-1] fp32: acceptance scores of draft positions 1..w-1 (finite; NaN not
+ * supported).  n_live: device int32 scalar (requests 0..n_live-1 are live), or NULL for
+ * all n_bs.  tokens / positions / kv_refs [n_bs, w] int32, each may be NULL (then the
+ * matching packed output is all fill, or not written if its pointer is NULL too).
+ * Outputs: k_init [n_bs] (may be NULL), k_out [n_bs], cu_slots [n_bs + 1],
+ * tokens_packed / pos_packed / ref_packed [m_cap] (each may be NULL), n_adjust (device
+ * int32 scalar, slots added or removed; may be NULL).  ws: at least 256 bytes, zeroed
+ * once (svp_workspace_init); n_live outside [0, n_bs] or budget > m_cap sets
+ * SVP_DEV_BAD_SLOTS and treats every request as inactive.
+ * Limits: 1 <= n_bs <= 2048, 2 <= w <= 16, 1 <= budget_per_req <= w, m_cap >= 1
+ * (SVP_EINVAL / SVP_EUNSUPPORTED otherwise).
+ */
+svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, int32_t w,
+                                 const int32_t *n_live, int32_t budget_per_req,
+                                 const int32_t *tokens, const int32_t *positions,
+                                 const int32_t *kv_refs, int32_t m_cap, int32_t fill_token,
+                                 int32_t fill_pos, int32_t fill_ref, int32_t *k_init,
+                                 int32_t *k_out, int32_t *cu_slots, int32_t *tokens_packed,
+                                 int32_t *pos_packed, int32_t *ref_packed, int32_t *n_adjust,
+                                 void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional
+from typing import Dict, Optional
 
 import torch
 
@@ -93,6 +93,12 @@ _SIGS = {
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "svp_margin_accept_workspace_size": (ctypes.c_int, [
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]),
+    "svp_dvl_allocate_pack": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_size_t, ctypes.c_void_p]),
     "svp_margin_accept": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -380,3 +386,47 @@ def margin_accept(logits, tokens, cu_slots, *, vocab: Optional[int] = None,
         _dev(acc, "accept_len", torch.int32), _dev(nxt, "next_token", torch.int32),
         ws.ptr, ws.nbytes, _stream(stream)), "svp_margin_accept")
     return outs
+
+
+def dvl_allocate_pack(scores, *, n_live=None, budget_per_req: int = 8, m_cap: Optional[int] = None,
+                      tokens=None, positions=None, kv_refs=None, fill_token: int = 0,
+                      fill_pos: int = 0, fill_ref: int = -1, ws: Optional[Workspace] = None,
+                      stream=None) -> Dict[str, torch.Tensor]:
+    """DVL budget allocator + flat-buffer packer (svp_dvl_allocate_pack).
+
+    scores [n_bs, w-1] fp32 acceptance scores; n_live: device int32 scalar tensor or None
+    (all live); tokens / positions / kv_refs [n_bs, w] int32 or None.  Returns k_init,
+    k, cu_slots, n_adjust and the packed fields that were given.
+    """
+    if scores.dim() != 2:
+        raise SvpError("scores must be [n_bs, w-1]")
+    n_bs, wm1 = scores.shape
+    w = wm1 + 1
+    dev = scores.device
+    if m_cap is None:
+        m_cap = w * n_bs
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(k_init=torch.empty(n_bs, **i32), k=torch.empty(n_bs, **i32),
+               cu_slots=torch.empty(n_bs + 1, **i32), n_adjust=torch.empty(1, **i32))
+    for name, f in (("tokens", tokens), ("positions", positions), ("kv_refs", kv_refs)):
+        if f is not None:
+            if tuple(f.shape) != (n_bs, w):
+                raise SvpError(f"{name} must be [n_bs, w]")
+            out[name] = torch.empty(m_cap, **i32)
+    if ws is None:
+        ws = _workspace(("dvl",), 256, dev, stream)
+    st = lib().svp_dvl_allocate_pack(
+        _dev(scores, "scores", torch.float32), n_bs, w,
+        _dev(n_live, "n_live", torch.int32) if n_live is not None else None, budget_per_req,
+        _dev(tokens, "tokens", torch.int32) if tokens is not None else None,
+        _dev(positions, "positions", torch.int32) if positions is not None else None,
+        _dev(kv_refs, "kv_refs", torch.int32) if kv_refs is not None else None,
+        m_cap, fill_token, fill_pos, fill_ref,
+        out["k_init"].data_ptr(), out["k"].data_ptr(), out["cu_slots"].data_ptr(),
+        out["tokens"].data_ptr() if "tokens" in out else None,
+        out["positions"].data_ptr() if "positions" in out else None,
+        out["kv_refs"].data_ptr() if "kv_refs" in out else None,
+        out["n_adjust"].data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "svp_dvl_allocate_pack")
+    out["ws"] = ws
+    return out

@@ -1,0 +1,106 @@
+"""GPU parity of svp_dvl_allocate_pack against the allocator / packer reference
+(oracle/dvl.py): integer outputs bit-exact ("DScale", SIII-C, Algorithm 1, Fig. 6)."""
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_verification_packed_gb300 as svp
+from oracle import dvl
+
+pytestmark = pytest.mark.gpu
+
+FIG6_GROW = [[1, 1, 1, 1, 0.6], [1] * 9 + [0.55], [1] * 6 + [0.52], [1] * 8 + [0.51]]
+
+
+def _scores(rows, w=16):
+    s = np.zeros((len(rows), w - 1), dtype=np.float32)
+    for i, r in enumerate(rows):
+        s[i, :len(r)] = r
+    return s
+
+
+def _run(s, n_live, per, m_cap, fields=True, seed=0, fills=(0, 0, -1), reference=True):
+    n_bs, wm1 = s.shape
+    w = wm1 + 1
+    rng = np.random.default_rng(seed)
+    tok = rng.integers(0, 250000, (n_bs, w)).astype(np.int32)
+    pos = rng.integers(0, 1 << 20, (n_bs, w)).astype(np.int32)
+    ref = rng.integers(0, 1 << 30, (n_bs, w)).astype(np.int32)
+    t = lambda a: torch.from_numpy(a).cuda()
+    nl = torch.tensor([n_live], dtype=torch.int32, device="cuda")
+    ws = svp.Workspace(256)
+    g = svp.dvl_allocate_pack(t(s), n_live=nl, budget_per_req=per, m_cap=m_cap,
+                              tokens=t(tok) if fields else None, positions=t(pos) if fields else None,
+                              kv_refs=t(ref) if fields else None, fill_token=fills[0], fill_pos=fills[1],
+                              fill_ref=fills[2], ws=ws)
+    torch.cuda.synchronize()
+    if not reference:
+        return g, None, ws
+    o = dvl.dvl_allocate_pack(s, n_live, per, m_cap, tok if fields else None, pos if fields else None,
+                              ref if fields else None, *fills)
+    return g, o, ws
+
+
+def _assert_same(g, o, fields=True):
+    assert g["k_init"].cpu().tolist() == o["k0"].tolist()
+    assert g["k"].cpu().tolist() == o["k"].tolist()
+    assert g["cu_slots"].cpu().tolist() == o["cu"].tolist()
+    assert int(g["n_adjust"].item()) == o["adjustments"]
+    if fields:
+        for name in ("tokens", "positions", "kv_refs"):
+            assert g[name].cpu().tolist() == o[name].tolist(), name
+
+
+def test_fig6_on_gpu():
+    g, o, ws = _run(_scores(FIG6_GROW), 4, 8, 64)
+    _assert_same(g, o)
+    assert g["k"].cpu().tolist() == [6, 10, 7, 9]
+    assert g["cu_slots"].cpu().tolist() == [0, 6, 16, 23, 32]
+    assert ws.read_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_batches_match_reference(seed):
+    rng = np.random.default_rng(1000 + seed)
+    n_bs = int(rng.choice([1, 3, 8, 64, 257, 1024, 2048]))
+    n_live = int(rng.integers(0, n_bs + 1))
+    per = int(rng.integers(1, 17))
+    kind = seed % 4
+    if kind == 0:
+        s = rng.random((n_bs, 15))
+    elif kind == 1:
+        s = rng.beta(0.4, 0.4, (n_bs, 15))
+    elif kind == 2:      # heavy ties: few distinct values
+        s = rng.integers(0, 5, (n_bs, 15)) / 4.0
+    else:                # sorted, near-threshold sums
+        s = np.sort(rng.random((n_bs, 15)), axis=1)[:, ::-1] * 1.02
+    s = s.astype(np.float32)
+    g, o, ws = _run(s, n_live, per, 16 * n_bs, seed=seed)
+    _assert_same(g, o)
+    assert ws.read_status() == 0
+
+
+@pytest.mark.parametrize("w", [2, 5, 16])
+def test_widths_and_extremes(w):
+    rng = np.random.default_rng(w)
+    n = 40
+    for s in (np.ones((n, w - 1)), np.zeros((n, w - 1)), rng.random((n, w - 1))):
+        for per in sorted({1, max(1, w // 2), w}):
+            g, o, ws = _run(s.astype(np.float32), n, per, w * n + 5, seed=w)
+            _assert_same(g, o)
+
+
+def test_no_fields_and_bad_live_count():
+    s = np.random.default_rng(3).random((16, 15)).astype(np.float32)
+    g, o, ws = _run(s, 10, 8, 160, fields=False)
+    _assert_same(g, o, fields=False)
+    assert ws.read_status() == 0
+    # more live requests than the bucket holds: status bit, everything inactive
+    g, _, ws = _run(s, 17, 8, 160, fields=True, reference=False)
+    assert ws.read_status() == svp.DEV_BAD_SLOTS
+    assert g["k"].cpu().tolist() == [0] * 16
+    assert g["cu_slots"].cpu().tolist() == [0] * 17
+    assert g["tokens"].cpu().tolist() == [0] * 160
+    # budget beyond m_cap
+    g, _, ws = _run(s, 10, 8, 79, fields=False, reference=False)
+    assert ws.read_status() == svp.DEV_BAD_SLOTS
