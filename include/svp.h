@@ -281,6 +281,19 @@ svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, int32_t w,
                                  int32_t *pos_packed, int32_t *ref_packed, int32_t *n_adjust,
                                  void *ws, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------------------------- */
+/* Row-mapped packing of a wide per-row field (DScale SIII-C, Flat-buffer packer: every  */
+/* field is packed with the same row mapping; SIII-D, fixed-address workspace).          */
+/*   dst row r = src row idx[r] for 0 <= idx[r] < src_rows, else zeros; r < rows.       */
+
+/*
+ * src [src_rows, row_bytes] and dst [rows, row_bytes] device buffers, 16-byte aligned,
+ * row_bytes a multiple of 16 (SVP_EUNSUPPORTED otherwise); idx [rows] int32 (e.g. the
+ * packed KV references of svp_dvl_allocate_pack).  No workspace.
+ */
+svp_status svp_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes,
+                           const int32_t *idx, int32_t rows, void *dst, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -99,6 +99,9 @@ _SIGS = {
         ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_size_t, ctypes.c_void_p]),
+    "svp_gather_rows": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32,
+        ctypes.c_void_p, ctypes.c_void_p]),
     "svp_margin_accept": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -429,4 +432,17 @@ def dvl_allocate_pack(scores, *, n_live=None, budget_per_req: int = 8, m_cap: Op
         out["n_adjust"].data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "svp_dvl_allocate_pack")
     out["ws"] = ws
+    return out
+
+
+def gather_rows(src, idx, *, out=None, stream=None):
+    """Packed copy of a wide per-row field (svp_gather_rows): out[r] = src[idx[r]] for
+    in-range ids, zeros otherwise.  src [src_rows, ...] contiguous; idx [rows] int32."""
+    rows = idx.shape[0]
+    if out is None:
+        out = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else out[0].numel() * out.element_size()
+    _check(lib().svp_gather_rows(_dev(src, "src"), src.shape[0], row_bytes,
+                                 _dev(idx, "idx", torch.int32), rows, _dev(out, "out"),
+                                 _stream(stream)), "svp_gather_rows")
     return out
