@@ -29,6 +29,12 @@ What it computes, with the passages it follows:
   budget, offsets, row-mapped packing with tail placeholders, and the retention measure
   of SIV.
 
+* ``stochastic`` (oracle/stochastic.py) -- the stochastic prefix verifier at temperature
+  T > 0 (DScale SIII-D, Prefix verifier): deterministic draft candidates accepted with the
+  target probability, the successor drawn from the target with the rejected candidate
+  removed (or unmodified after a full accept), random numbers given as inputs; plus the
+  exact output law of one request.
+
 Pins (tests/test_oracle_*.py): brute force on tiny inputs, closed forms, the packed vs
 alone / relayout / paged vs contiguous / permutation invariants, numpy argmax and sort
 on planted ties, exhaustive accept patterns, and the worked examples the pages print
