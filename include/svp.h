@@ -294,6 +294,35 @@ svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, int32_t w,
 svp_status svp_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes,
                            const int32_t *idx, int32_t rows, void *dst, void *stream);
 
+/* ---------------------------------------------------------------------------------- */
+/* Stochastic prefix verifier, temperature T > 0 (DScale SIII-D, Prefix verifier).       */
+/*   P_r = softmax(logits[r] / T).  Candidate j of request i (tokens[off_i + j],          */
+/*   1 <= j < k_i) is accepted iff u_accept[off_i + j] < P_{off_i+j-1}(candidate), in     */
+/*   order; the first rejection ends the prefix.  a_i = accepted candidates;              */
+/*   accept_len[i] = 1 + a_i.  The successor next_token[i] is the smallest token y with   */
+/*   sum_{y' <= y} w(y') > u_next[i] * sum w, over row off_i + a_i with weights          */
+/*   w = P_{off_i+a_i}, the rejected candidate's weight set to 0 (none removed when every */
+/*   candidate passed).  k_i = 0: accept_len 0, next_token -1.  The row softmax is       */
+/*   evaluated in fp32 (exp2 of scaled differences), so a draw within rounding of a      */
+/*   boundary may fall on either side.                                                    */
+
+svp_status svp_stochastic_accept_workspace_size(int32_t m_cap, int32_t vocab, size_t *bytes);
+
+/*
+ * logits [m_cap, row_stride] (dtype), vocab <= row_stride; tokens [m_cap] int32;
+ * cu_slots [n+1]; u_accept [m_cap] fp32 and u_next [n] fp32, uniform draws in [0, 1)
+ * supplied by the caller; outputs accept_len [n], next_token [n] int32 and p_draft [m_cap]
+ * (the acceptance probability of each tested candidate; may be NULL).  Rows >=
+ * cu_slots[n] are not read.  Invalid cu_slots set SVP_DEV_BAD_SLOTS; the request gets
+ * accept_len 0 and next_token -1.
+ */
+svp_status svp_stochastic_accept(const void *logits, int64_t row_stride, int32_t m_cap,
+                                 int32_t vocab, svp_dtype dtype, const int32_t *tokens,
+                                 const int32_t *cu_slots, int32_t n, float temperature,
+                                 const float *u_accept, const float *u_next,
+                                 int32_t *accept_len, int32_t *next_token, float *p_draft,
+                                 void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -102,6 +102,13 @@ _SIGS = {
     "svp_gather_rows": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32,
         ctypes.c_void_p, ctypes.c_void_p]),
+    "svp_stochastic_accept_workspace_size": (ctypes.c_int, [
+        ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]),
+    "svp_stochastic_accept": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_size_t, ctypes.c_void_p]),
     "svp_margin_accept": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -446,3 +453,36 @@ def gather_rows(src, idx, *, out=None, stream=None):
                                  _dev(idx, "idx", torch.int32), rows, _dev(out, "out"),
                                  _stream(stream)), "svp_gather_rows")
     return out
+
+
+def stochastic_accept_workspace_size(m_cap: int, vocab: int) -> int:
+    nb = ctypes.c_size_t(0)
+    _check(lib().svp_stochastic_accept_workspace_size(m_cap, vocab, ctypes.byref(nb)),
+           "svp_stochastic_accept_workspace_size")
+    return int(nb.value)
+
+
+def stochastic_accept(logits, tokens, cu_slots, u_accept, u_next, *, temperature: float,
+                      vocab: Optional[int] = None, ws: Optional[Workspace] = None, outs=None,
+                      stream=None):
+    """Stochastic prefix verifier (svp_stochastic_accept); returns (accept_len [n],
+    next_token [n], p_draft [m_cap])."""
+    m_cap, stride = logits.shape
+    vocab = stride if vocab is None else vocab
+    n = cu_slots.shape[0] - 1
+    dev = logits.device
+    if outs is None:
+        outs = (torch.empty(n, dtype=torch.int32, device=dev),
+                torch.empty(n, dtype=torch.int32, device=dev),
+                torch.full((m_cap,), float("nan"), dtype=torch.float32, device=dev))
+    acc, nxt, pd = outs
+    if ws is None:
+        ws = _workspace(("stochastic",), stochastic_accept_workspace_size(m_cap, vocab), dev, stream)
+    _check(lib().svp_stochastic_accept(
+        _dev(logits, "logits"), stride, m_cap, vocab, _dtype_code(logits),
+        _dev(tokens, "tokens", torch.int32), _dev(cu_slots, "cu_slots", torch.int32), n,
+        float(temperature), _dev(u_accept, "u_accept", torch.float32),
+        _dev(u_next, "u_next", torch.float32), _dev(acc, "accept_len", torch.int32),
+        _dev(nxt, "next_token", torch.int32), _dev(pd, "p_draft", torch.float32) if pd is not None else None,
+        ws.ptr, ws.nbytes, _stream(stream)), "svp_stochastic_accept")
+    return outs

@@ -1,0 +1,117 @@
+"""GPU parity of svp_stochastic_accept against the fp64 stochastic prefix verifier
+(oracle/stochastic.py), "DScale" SIII-D.  Decisions are compared exactly except where a
+uniform draw lies within rounding of its boundary (then either side is valid and the
+GPU's choice is checked against the oracle's bracket); acceptance probabilities to 2e-5;
+the output law of many replicated requests against the exact law (chi-square)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_packed_gb300 as svp
+from oracle import stochastic as st
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-5
+
+
+def _batch(seed, n, V, dtype, kmax=16):
+    rng = np.random.default_rng(seed)
+    ks = rng.integers(0, kmax + 1, n)
+    ks[rng.integers(0, n)] = kmax
+    cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    m = int(cu[-1]) + 3
+    z = torch.randn(m, V, generator=torch.Generator().manual_seed(seed)) * 2.0
+    z = z.to(dtype)
+    zf = z.float().numpy().astype(np.float64)
+    am = zf.argmax(axis=1)
+    tok = rng.integers(0, V, m).astype(np.int32)
+    for i in range(n):
+        for j in range(1, int(ks[i])):
+            if rng.random() < 0.6:
+                tok[cu[i] + j] = am[cu[i] + j - 1]
+    ua = rng.random(m).astype(np.float32)
+    un = rng.random(n).astype(np.float32)
+    return z, zf, tok, cu, ua, un
+
+
+def _borderline(zf, tok, cu, T, ua, un, i, y_gpu):
+    """True when request i's outcome sits within TOL of a decision boundary."""
+    off, k = int(cu[i]), int(cu[i + 1] - cu[i])
+    a, excl = 0, -1
+    for j in range(1, k):
+        p = st.row_probs(zf[off + j - 1], T)[int(tok[off + j])]
+        if abs(float(ua[off + j]) - p) < TOL:
+            return True
+        if ua[off + j] < p:
+            a += 1
+        else:
+            excl = int(tok[off + j])
+            break
+    p = st.row_probs(zf[off + a], T)
+    w = p.copy()
+    if excl >= 0:
+        w[excl] = 0.0
+    c = np.cumsum(w) / w.sum()
+    t = float(un[i])
+    lo = c[y_gpu - 1] if y_gpu > 0 else 0.0
+    return lo - TOL <= t <= c[y_gpu] + TOL
+
+
+@pytest.mark.parametrize("case", [(0, 8, 512, torch.bfloat16, 1.0), (1, 20, 10000, torch.bfloat16, 0.7),
+                                  (2, 6, 40000, torch.bfloat16, 1.5), (3, 12, 3000, torch.float32, 1.0)])
+def test_matches_reference(case):
+    seed, n, V, dtype, T = case
+    z, zf, tok, cu, ua, un = _batch(seed, n, V, dtype)
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    ws = svp.Workspace(svp.stochastic_accept_workspace_size(z.shape[0], V))
+    acc, nxt, pd = svp.stochastic_accept(z.cuda(), d(tok), d(cu), d(ua), d(un), temperature=T, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0
+    o_acc, o_nxt, o_pd = st.stochastic_accept(zf, tok, cu, T, ua.astype(np.float64), un.astype(np.float64))
+    acc, nxt, pd = acc.cpu().numpy(), nxt.cpu().numpy(), pd.cpu().numpy()
+    tested = ~np.isnan(o_pd) & ~np.isnan(pd)
+    assert np.abs(pd[tested] - o_pd[tested]).max() <= TOL
+    mism = 0
+    for i in range(n):
+        if acc[i] != o_acc[i] or nxt[i] != o_nxt[i]:
+            mism += 1
+            assert _borderline(zf, tok, cu, T, ua, un, i, int(nxt[i])), (i, acc[i], o_acc[i], nxt[i], o_nxt[i])
+    assert mism <= max(1, n // 50)
+    assert set(np.where(np.diff(cu) == 0)[0].tolist()) <= set(np.where(acc == 0)[0].tolist())
+
+
+def test_low_temperature_equals_greedy():
+    n, V = 16, 4096
+    z, zf, tok, cu, ua, un = _batch(7, n, V, torch.bfloat16)
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    acc, nxt, _ = svp.stochastic_accept(z.cuda(), d(tok), d(cu), d(ua), d(un), temperature=1e-4)
+    idx, _, _, _ = oracle.row_top2(z)
+    g_acc, g_nxt = oracle.greedy_accept(idx, tok, cu)
+    assert acc.cpu().tolist() == g_acc.tolist()
+    assert nxt.cpu().tolist() == g_nxt.tolist()
+
+
+def test_output_law_of_replicated_requests():
+    rng = np.random.default_rng(11)
+    V, k, T, reps = 6, 3, 1.0, 20000
+    zr = rng.normal(0, 1.0, (k, V))
+    drafts = np.array([0, int(np.argmax(zr[0])), int(np.argsort(zr[1])[-2])], dtype=np.int32)
+    z = torch.from_numpy(np.tile(zr, (reps, 1)).astype(np.float32))
+    tok = np.tile(drafts, reps)
+    cu = np.arange(0, k * reps + 1, k).astype(np.int32)
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    acc, nxt, _ = svp.stochastic_accept(z.cuda(), d(tok), d(cu), d(rng.random(k * reps).astype(np.float32)),
+                                        d(rng.random(reps).astype(np.float32)), temperature=T)
+    law = st.output_distribution(z.numpy()[:k].astype(np.float64), drafts, T)
+    counts = {}
+    for a, y in zip(acc.cpu().numpy() - 1, nxt.cpu().numpy()):
+        counts[(int(a), int(y))] = counts.get((int(a), int(y)), 0) + 1
+    assert set(counts) <= set(law)
+    chi2, dof = 0.0, 0
+    for key, pr in law.items():
+        e = pr * reps
+        if e >= 5:
+            chi2 += (counts.get(key, 0) - e) ** 2 / e
+            dof += 1
+    assert chi2 < (dof - 1) + 4 * np.sqrt(2 * (dof - 1)) + 10, (chi2, dof)
