@@ -35,6 +35,10 @@ What it computes, with the passages it follows:
   removed (or unmodified after a full accept), random numbers given as inputs; plus the
   exact output law of one request.
 
+* ``features`` (oracle/features.py) -- the 18 draft-signal values per draft-logit row
+  (DScale SIII-C, Acceptance predictor) and DFlash7-ACT margin-threshold truncation
+  (DFlash-Mini-Lab README).
+
 Pins (tests/test_oracle_*.py): brute force on tiny inputs, closed forms, the packed vs
 alone / relayout / paged vs contiguous / permutation invariants, numpy argmax and sort
 on planted ties, exhaustive accept patterns, and the worked examples the pages print
