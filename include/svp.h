@@ -323,6 +323,32 @@ svp_status svp_stochastic_accept(const void *logits, int64_t row_stride, int32_t
                                  int32_t *accept_len, int32_t *next_token, float *p_draft,
                                  void *ws, size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------------------------- */
+/* Draft-signal features (DScale SIII-C, Acceptance predictor).  For every row of draft  */
+/* logits, 18 fp32 values: [0] the highest logit; [1..15] its gaps to ranks 2..16 (rank r */
+/* = r-th element of the row sorted descending as a multiset, gap = top1 - rank_r in     */
+/* fp32); [16] the top token's log-probability (top1 - log-sum-exp of the row); [17] the  */
+/* entropy -sum p ln p of softmax(row).  Sums are fp32.                                    */
+
+svp_status svp_draft_features_workspace_size(int32_t rows, int32_t vocab, size_t *bytes);
+
+/*
+ * logits [rows, row_stride] (dtype), 16 <= vocab <= row_stride; features [rows, 18] fp32.
+ * ws zeroed once (svp_workspace_init); the kernel leaves its tickets at zero.
+ */
+svp_status svp_draft_features(const void *logits, int64_t row_stride, int32_t rows,
+                              int32_t vocab, svp_dtype dtype, float *features, void *ws,
+                              size_t ws_bytes, void *stream);
+
+/* ACT truncation (DFlash-Mini-Lab README, DFlash7-ACT): the draft suffix of request i is  */
+/* cut before its first position j (1 <= j < w) whose margin is below `threshold`;       */
+/* k_out[i] = 1 + the number of positions kept (threshold 0 keeps the full block w).      */
+/* margins: element ((i * (w-1) + j - 1) * stride) is the margin of position j of request */
+/* i (stride = 1 for svp_draft_margin's margin array, 18 with features + 1).  No         */
+/* workspace.                                                                             */
+svp_status svp_act_truncate(const float *margins, int64_t stride, int32_t n, int32_t w,
+                            float threshold, int32_t *k_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -109,6 +109,14 @@ _SIGS = {
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_size_t, ctypes.c_void_p]),
+    "svp_draft_features_workspace_size": (ctypes.c_int, [
+        ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]),
+    "svp_draft_features": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "svp_act_truncate": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+        ctypes.c_void_p, ctypes.c_void_p]),
     "svp_margin_accept": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -486,3 +494,35 @@ def stochastic_accept(logits, tokens, cu_slots, u_accept, u_next, *, temperature
         _dev(nxt, "next_token", torch.int32), _dev(pd, "p_draft", torch.float32) if pd is not None else None,
         ws.ptr, ws.nbytes, _stream(stream)), "svp_stochastic_accept")
     return outs
+
+
+def draft_features_workspace_size(rows: int, vocab: int) -> int:
+    nb = ctypes.c_size_t(0)
+    _check(lib().svp_draft_features_workspace_size(rows, vocab, ctypes.byref(nb)),
+           "svp_draft_features_workspace_size")
+    return int(nb.value)
+
+
+def draft_features(logits, *, vocab: Optional[int] = None, out=None, ws: Optional[Workspace] = None,
+                   stream=None):
+    """[rows, 18] fp32 draft-signal features of every logit row (svp_draft_features)."""
+    rows, stride = logits.shape
+    vocab = stride if vocab is None else vocab
+    if out is None:
+        out = torch.empty(rows, 18, dtype=torch.float32, device=logits.device)
+    if ws is None:
+        ws = _workspace(("features",), draft_features_workspace_size(rows, vocab), logits.device, stream)
+    _check(lib().svp_draft_features(_dev(logits, "logits"), stride, rows, vocab, _dtype_code(logits),
+                                    _dev(out, "features", torch.float32), ws.ptr, ws.nbytes,
+                                    _stream(stream)), "svp_draft_features")
+    return out
+
+
+def act_truncate(margins, *, n: int, w: int, threshold: float, stride: int = 1, out=None, stream=None):
+    """k [n] int32 after ACT truncation of margins laid out per request and position."""
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=margins.device)
+    _check(lib().svp_act_truncate(_dev(margins, "margins", torch.float32), stride, n, w,
+                                  float(threshold), _dev(out, "k", torch.int32), _stream(stream)),
+           "svp_act_truncate")
+    return out

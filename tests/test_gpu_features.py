@@ -1,0 +1,52 @@
+"""GPU parity of svp_draft_features / svp_act_truncate against oracle/features.py
+("DScale" SIII-C Acceptance predictor; DFlash-Mini-Lab DFlash7-ACT).  The top logit is a
+stored value (bit-exact); the gaps are fp32 differences of stored values (within one fp32
+rounding of the fp64 reference); log-probability and entropy come from fp32 sums (bars
+below).  ACT decisions are bit-exact given the same margins."""
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_verification_packed_gb300 as svp
+from oracle import features as ft
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("case", [(0, 40, 300, torch.bfloat16, 0), (1, 17, 1001, torch.float32, 0),
+                                  (2, 12, 10000, torch.bfloat16, 8), (3, 9, 248320, torch.bfloat16, 0),
+                                  (4, 6, 40007, torch.float32, 3)])
+def test_features_match_reference(case):
+    seed, rows, V, dtype, pad = case
+    g = torch.Generator().manual_seed(seed)
+    z = (torch.randn(rows, V + pad, generator=g) * 2.0).to(dtype)
+    z[1, 7] = z[1].max() + 1.0
+    z[1, 70] = z[1, 7]                    # repeated maximum: gap 2 = 0
+    ref = ft.draft_features(z.float().numpy()[:, :V].astype(np.float64))
+    ws = svp.Workspace(svp.draft_features_workspace_size(rows, V))
+    out = svp.draft_features(z.cuda(), vocab=V, ws=ws).cpu().numpy().astype(np.float64)
+    assert out[:, 0].tolist() == ref[:, 0].tolist()
+    assert np.all(np.abs(out[:, 1:16] - ref[:, 1:16]) <= 6e-8 * np.maximum(np.abs(ref[:, 1:16]), np.abs(ref[:, :1])))
+    assert out[1, 1] == 0.0
+    assert np.abs(out[:, 16] - ref[:, 16]).max() <= 1e-4
+    assert np.abs(out[:, 17] - ref[:, 17]).max() <= 1e-4 * max(1.0, np.log(V))
+    # the workspace tickets are back at zero: a second call on the same workspace agrees
+    out2 = svp.draft_features(z.cuda(), vocab=V, ws=ws).cpu().numpy().astype(np.float64)
+    assert np.array_equal(out, out2)
+
+
+def test_act_truncation():
+    rng = np.random.default_rng(5)
+    n, w, V = 32, 16, 4096
+    z = (torch.randn(n * (w - 1), V) * 2.0).to(torch.bfloat16)
+    feats = svp.draft_features(z.cuda())
+    margins = feats[:, 1].contiguous()
+    mg = margins.cpu().numpy().reshape(n, w - 1)
+    for thr in (0.0, 0.25, 0.5, 1.0, 1.5, 2.0, 1e9):
+        # stride 18 with the margin column: pass a view starting at column 1
+        k = svp.act_truncate(feats.view(-1)[1:].contiguous(), n=n, w=w, threshold=thr, stride=18)
+        k1 = svp.act_truncate(margins, n=n, w=w, threshold=thr, stride=1)
+        expect = ft.act_truncate(mg, thr)
+        assert k.cpu().tolist() == expect.tolist()
+        assert k1.cpu().tolist() == expect.tolist()
+    assert svp.act_truncate(margins, n=n, w=w, threshold=0.0).cpu().tolist() == [w] * n
