@@ -10,8 +10,10 @@
 //   * Each logits row is cut into equal chunks of <= 8192 elements; every warp is an
 //     independent worker on one (row, chunk) unit at a time (no CTA barriers).
 //   * Each lane keeps a (top1, top1_idx, top2) triple over 16-byte vector loads, eight
-//     in flight at once; a vector whose maximum cannot beat the current top-2 is
-//     skipped after one packed max.
+//     in flight at once, updated without branches (a skip test on the lane's own top-2
+//     diverges across the warp on nearly every vector of a chunk): top2 = max(top2,
+//     min(top1, x)), top1 = max(top1, x), and the index moves only on a strictly larger
+//     value, so it keeps the lane's first occurrence of its maximum.
 //   * Triples merge by warp shuffles; the merge is commutative and associative (ties:
 //     lowest index), so results do not depend on arrival order.
 //   * The warp that finishes the last chunk of a row (atomic ticket, no waiting)
@@ -34,6 +36,15 @@ struct Top2 {
 };
 
 __device__ __forceinline__ Top2 top2_identity() { return Top2{-INFINITY, -INFINITY, INT_MAX}; }
+
+// Insert element (x, idx) without branches; indices reach a triple in increasing order,
+// so the first occurrence of the maximum keeps its index.
+__device__ __forceinline__ void top2_push_nb(Top2 &t, float x, int32_t idx)
+{
+    t.v2 = fmaxf(t.v2, fminf(t.v1, x));
+    t.i1 = (x > t.v1 || t.i1 == INT_MAX) ? idx : t.i1;   // the lane's first element seeds it
+    t.v1 = fmaxf(t.v1, x);
+}
 
 // Insert element (x, idx); indices reach a given triple in increasing order.
 __device__ __forceinline__ void top2_push(Top2 &t, float x, int32_t idx)
@@ -159,29 +170,19 @@ __device__ __forceinline__ Top2 scan_chunk_warp(const MarginArgs &a, int64_t row
                     break;
                 const int32_t e0 = c0 + v * VW;
                 if (kBf16) {
-                    const uint32_t m4 = bf16x2_max(bf16x2_max(buf[u].x, buf[u].y),
-                                                   bf16x2_max(buf[u].z, buf[u].w));
-                    const float m8 = fmaxf(bf16_lo(m4), bf16_hi(m4));
-                    if (m8 > t.v2 || t.i1 == INT_MAX) {
-                        top2_push(t, bf16_lo(buf[u].x), e0 + 0);
-                        top2_push(t, bf16_hi(buf[u].x), e0 + 1);
-                        top2_push(t, bf16_lo(buf[u].y), e0 + 2);
-                        top2_push(t, bf16_hi(buf[u].y), e0 + 3);
-                        top2_push(t, bf16_lo(buf[u].z), e0 + 4);
-                        top2_push(t, bf16_hi(buf[u].z), e0 + 5);
-                        top2_push(t, bf16_lo(buf[u].w), e0 + 6);
-                        top2_push(t, bf16_hi(buf[u].w), e0 + 7);
-                    }
+                    top2_push_nb(t, bf16_lo(buf[u].x), e0 + 0);
+                    top2_push_nb(t, bf16_hi(buf[u].x), e0 + 1);
+                    top2_push_nb(t, bf16_lo(buf[u].y), e0 + 2);
+                    top2_push_nb(t, bf16_hi(buf[u].y), e0 + 3);
+                    top2_push_nb(t, bf16_lo(buf[u].z), e0 + 4);
+                    top2_push_nb(t, bf16_hi(buf[u].z), e0 + 5);
+                    top2_push_nb(t, bf16_lo(buf[u].w), e0 + 6);
+                    top2_push_nb(t, bf16_hi(buf[u].w), e0 + 7);
                 } else {
-                    const float x0 = __uint_as_float(buf[u].x), x1 = __uint_as_float(buf[u].y);
-                    const float x2 = __uint_as_float(buf[u].z), x3 = __uint_as_float(buf[u].w);
-                    const float m4 = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-                    if (m4 > t.v2 || t.i1 == INT_MAX) {
-                        top2_push(t, x0, e0 + 0);
-                        top2_push(t, x1, e0 + 1);
-                        top2_push(t, x2, e0 + 2);
-                        top2_push(t, x3, e0 + 3);
-                    }
+                    top2_push_nb(t, __uint_as_float(buf[u].x), e0 + 0);
+                    top2_push_nb(t, __uint_as_float(buf[u].y), e0 + 1);
+                    top2_push_nb(t, __uint_as_float(buf[u].z), e0 + 2);
+                    top2_push_nb(t, __uint_as_float(buf[u].w), e0 + 3);
                 }
             }
         }
@@ -326,7 +327,7 @@ struct MarginPlan {
 static MarginPlan margin_plan(int32_t rows, int32_t vocab, int32_t n)
 {
     MarginPlan p{};
-    const int32_t target = 8192;   // elements per unit (16 KB of bf16), one warp each
+    const int32_t target = 16384;  // elements per unit (32 KB of bf16), one warp each
     p.chunks_per_row = (vocab + target - 1) / target;
     if (p.chunks_per_row < 1)
         p.chunks_per_row = 1;

@@ -82,7 +82,16 @@ def test_noalloc_matches_workspace_entry_point_twice(case):
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     fn = _noalloc_fn()
-    # 8192 rows x 262144 vocabulary needs far more than the fixed 2 MiB of scratch; the
-    # call is refused on the host before anything is enqueued (pointers never touched)
-    rc = fn(16, 262144, 8192, 262144, svp.SVP_BF16, 16, 16, 64, 16, 16, 16, 16, 16, 16, None)
+    rows, vocab, n = 65536, 262144, 64
+    # the sizes must need more than the fixed 2 MiB of scratch, checked through the
+    # workspace query first, so the call below is refused on the host and never enqueues
+    # anything; the buffers are real but far too small for these sizes
+    need = svp.margin_accept_workspace_size(n, rows, vocab)
+    assert need > (2 << 20) * 4
+    small_i = torch.zeros(64, dtype=torch.int32, device="cuda")
+    small_f = torch.zeros(64, dtype=torch.float32, device="cuda")
+    logits = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    p = lambda t: t.data_ptr()
+    rc = fn(p(logits), vocab, rows, vocab, svp.SVP_BF16, p(small_i), p(small_i), n, p(small_i),
+            p(small_f), p(small_f), p(small_f), p(small_i), p(small_i), None)
     assert rc == svp.SVP_EWORKSPACE
