@@ -11,9 +11,11 @@
 //     independent worker on one (row, chunk) unit at a time (no CTA barriers).
 //   * Each lane keeps a (top1, top1_idx, top2) triple over 16-byte vector loads, eight
 //     in flight at once, updated without branches (a skip test on the lane's own top-2
-//     diverges across the warp on nearly every vector of a chunk): top2 = max(top2,
-//     min(top1, x)), top1 = max(top1, x), and the index moves only on a strictly larger
-//     value, so it keeps the lane's first occurrence of its maximum.
+//     diverges across the warp on nearly every vector of a chunk).  bf16 rows: packed
+//     bf16x2 min/max over two interleaved streams, the lane maximum per vector with the
+//     first vector that reached it, whose element index is recovered at the end; fp32
+//     rows: top2 = max(top2, min(top1, x)), top1 = max(top1, x), the index moving only
+//     on a strictly larger value (the lane's first occurrence of its maximum).
 //   * Triples merge by warp shuffles; the merge is commutative and associative (ties:
 //     lowest index), so results do not depend on arrival order.
 //   * The warp that finishes the last chunk of a row (atomic ticket, no waiting)
@@ -84,6 +86,14 @@ __device__ __forceinline__ Top2 top2_warp_merge(Top2 t)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a);
+    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162 *>(&b);
+    __nv_bfloat162 z = __hmin2(x, y);
+    return *reinterpret_cast<uint32_t *>(&z);
+}
+
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
 {
     __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a);
@@ -119,7 +129,17 @@ struct MarginArgs {
 };
 
 constexpr int kMarginThreads = 256;      // 8 independent warps per CTA
-constexpr int kMarginBatch = 8;          // 16-byte loads in flight per lane
+constexpr int kMarginBatch = 8;          // 16-byte loads in flight per lane (fallback path)
+constexpr int kMarginStages = 16;        // async-copy ring: 16-byte vectors in flight per lane
+constexpr int kMarginSmem = (kMarginThreads / 32) * kMarginStages * 32 * 16;   // 64 KB
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 
 // Which request owns packed row r (cu_slots non-decreasing, validated by the caller).
@@ -147,7 +167,7 @@ __device__ __forceinline__ float load_elem(const MarginArgs &a, int64_t row, int
 // One warp scans elements [c0, c1) of a row; lane-local triples, indices increasing.
 template <bool kBf16>
 __device__ __forceinline__ Top2 scan_chunk_warp(const MarginArgs &a, int64_t row, int32_t c0,
-                                                int32_t c1, int lane)
+                                                int32_t c1, int lane, uint8_t *ring_base)
 {
     Top2 t = top2_identity();
     constexpr int VW = kBf16 ? 8 : 4;        // elements per 16-byte vector
@@ -156,29 +176,74 @@ __device__ __forceinline__ Top2 scan_chunk_warp(const MarginArgs &a, int64_t row
         const int32_t nvec = (c1 - c0) / VW;
         const uint4 *vp = reinterpret_cast<const uint4 *>(
             reinterpret_cast<const uint8_t *>(a.logits) + (row * a.row_stride + c0) * (kBf16 ? 2 : 4));
-        for (int32_t v0 = 0; v0 < nvec; v0 += 32 * kMarginBatch) {
-            uint4 buf[kMarginBatch];
-#pragma unroll
-            for (int u = 0; u < kMarginBatch; ++u) {
-                const int32_t v = v0 + u * 32 + lane;
-                buf[u] = (v < nvec) ? __ldcs(vp + v) : make_uint4(0, 0, 0, 0);
+        if (kBf16) {
+            // two interleaved streams per lane (even / odd elements of each bf16 pair), each
+            // with a packed (top1, top2): 3 bf16x2 min/max per pair of elements.  The lane's
+            // maximum is tracked per vector with the first vector that reached it; the
+            // element index is recovered from that vector at the end.
+            uint32_t p1 = 0xff80ff80u, p2 = 0xff80ff80u;
+            float vmax = -INFINITY;
+            int32_t pos = -1;
+            // each lane streams its own vectors v = lane, lane + 32, ... through a ring of
+            // kMarginStages 16-byte slots (cp.async; every lane reads only what it copied)
+            const uint32_t ring = smem_u32(ring_base) + lane * 16;
+            for (int st = 0; st < kMarginStages; ++st) {
+                const int32_t v = st * 32 + lane;
+                if (v < nvec)
+                    cp_async16(ring + st * 512, vp + v);
+                cp_async_commit();
             }
+            for (int32_t k = 0; k * 32 + lane < nvec; ++k) {
+                cp_async_wait<kMarginStages - 1>();
+                const int32_t v = k * 32 + lane;
+                const uint32_t slot = ring + (k % kMarginStages) * 512;
+                const int4 x = ld_shared_i4(slot);
+                const uint32_t w[4] = {(uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w};
 #pragma unroll
-            for (int u = 0; u < kMarginBatch; ++u) {
-                const int32_t v = v0 + u * 32 + lane;
-                if (v >= nvec)
-                    break;
-                const int32_t e0 = c0 + v * VW;
-                if (kBf16) {
-                    top2_push_nb(t, bf16_lo(buf[u].x), e0 + 0);
-                    top2_push_nb(t, bf16_hi(buf[u].x), e0 + 1);
-                    top2_push_nb(t, bf16_lo(buf[u].y), e0 + 2);
-                    top2_push_nb(t, bf16_hi(buf[u].y), e0 + 3);
-                    top2_push_nb(t, bf16_lo(buf[u].z), e0 + 4);
-                    top2_push_nb(t, bf16_hi(buf[u].z), e0 + 5);
-                    top2_push_nb(t, bf16_lo(buf[u].w), e0 + 6);
-                    top2_push_nb(t, bf16_hi(buf[u].w), e0 + 7);
-                } else {
+                for (int h = 0; h < 4; ++h) {
+                    p2 = bf16x2_max(p2, bf16x2_min(p1, w[h]));
+                    p1 = bf16x2_max(p1, w[h]);
+                }
+                const uint32_t m4 = bf16x2_max(bf16x2_max(w[0], w[1]), bf16x2_max(w[2], w[3]));
+                const float m8 = fmaxf(bf16_lo(m4), bf16_hi(m4));
+                const bool take = m8 > vmax || pos < 0;
+                pos = take ? v : pos;
+                vmax = take ? fmaxf(vmax, m8) : vmax;
+                // the slot is refilled only after its value has been consumed
+                const int32_t vn = v + kMarginStages * 32;
+                if (vn < nvec)
+                    cp_async16(slot, vp + vn);
+                cp_async_commit();
+            }
+            cp_async_wait<0>();
+            if (pos >= 0) {
+                const float a1 = bf16_lo(p1), b1 = bf16_hi(p1);
+                t.v1 = fmaxf(a1, b1);
+                t.v2 = fmaxf(fminf(a1, b1), fmaxf(bf16_lo(p2), bf16_hi(p2)));
+                const uint4 x = __ldg(vp + pos);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                int32_t j = 7;
+#pragma unroll
+                for (int h = 3; h >= 0; --h) {
+                    j = bf16_hi(w[h]) == t.v1 ? 2 * h + 1 : j;
+                    j = bf16_lo(w[h]) == t.v1 ? 2 * h : j;
+                }
+                t.i1 = c0 + pos * VW + j;
+            }
+        } else {
+            for (int32_t v0 = 0; v0 < nvec; v0 += 32 * kMarginBatch) {
+                uint4 buf[kMarginBatch];
+#pragma unroll
+                for (int u = 0; u < kMarginBatch; ++u) {
+                    const int32_t v = v0 + u * 32 + lane;
+                    buf[u] = (v < nvec) ? __ldcs(vp + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < kMarginBatch; ++u) {
+                    const int32_t v = v0 + u * 32 + lane;
+                    if (v >= nvec)
+                        break;
+                    const int32_t e0 = c0 + v * VW;
                     top2_push_nb(t, __uint_as_float(buf[u].x), e0 + 0);
                     top2_push_nb(t, __uint_as_float(buf[u].y), e0 + 1);
                     top2_push_nb(t, __uint_as_float(buf[u].z), e0 + 2);
@@ -209,7 +274,9 @@ __device__ void finish_request(const MarginArgs &a, int32_t i)
 template <bool kBf16>
 __global__ void __launch_bounds__(kMarginThreads) margin_kernel(MarginArgs a)
 {
+    extern __shared__ __align__(16) uint8_t margin_smem[];
     const int lane = threadIdx.x & 31;
+    uint8_t *ring_base = margin_smem + (threadIdx.x >> 5) * (kMarginStages * 512);
     const int64_t gwarp = ((int64_t)blockIdx.x * kMarginThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kMarginThreads) >> 5;
 
@@ -236,7 +303,7 @@ __global__ void __launch_bounds__(kMarginThreads) margin_kernel(MarginArgs a)
         const int32_t ch = (int32_t)(w % a.chunks_per_row);
         const int32_t c0 = ch * a.chunk;
         const int32_t c1 = min(a.vocab, c0 + a.chunk);
-        Top2 t = top2_warp_merge(scan_chunk_warp<kBf16>(a, row, c0, c1, lane));
+        Top2 t = top2_warp_merge(scan_chunk_warp<kBf16>(a, row, c0, c1, lane, ring_base));
         int last = 0;
         if (lane == 0) {
             a.partial[row * a.chunks_per_row + ch] = t;
@@ -407,10 +474,19 @@ svp_status margin_launch(const void *logits, int64_t row_stride, int32_t rows, i
         grid = (int64_t)sm_count() * 8;
     if (grid < 1)
         grid = 1;
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(margin_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMarginSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(margin_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMarginSmem) != cudaSuccess)
+            return SVP_ECUDA;
+        configured = true;
+    }
     if (dtype == SVP_BF16)
-        margin_kernel<true><<<(unsigned)grid, kMarginThreads, 0, stream>>>(a);
+        margin_kernel<true><<<(unsigned)grid, kMarginThreads, kMarginSmem, stream>>>(a);
     else
-        margin_kernel<false><<<(unsigned)grid, kMarginThreads, 0, stream>>>(a);
+        margin_kernel<false><<<(unsigned)grid, kMarginThreads, kMarginSmem, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
 }
 
