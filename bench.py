@@ -515,6 +515,7 @@ def run_ours(args):
         extras["prefill_4096_causal"] = {"us": round(pms * 1e3, 1),
                                          "tflops": round(flops / (pms / 1e3) / 1e12, 1),
                                          "frac_of_bf16_peak": round(flops / (pms / 1e3) / 1e12 / tf_peak, 4)}
+        extras.update(next_rows_extras(svp, dev))
         result["extras"] = extras
 
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -526,6 +527,120 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def graph_us(fn, reps: int = 100) -> float:
+    """Device time of one call of fn (CUDA-graph replay, events on the replay stream)."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps * 1e3
+
+
+def next_rows_extras(svp, dev):
+    """The allocator/packer, the captured step, the stochastic verifier and the draft
+    features, each timed by graph replay (device time per call)."""
+    import numpy as np
+    import torch
+    from speculative_decoding_verification_packed_gb300 import workloads as wl
+    from speculative_decoding_verification_packed_gb300.pipeline import VerifyPipeline
+    out = {}
+    # DVL allocator + packer: budget 8N over W = 16, three batch sizes; retention of the
+    # windows for labels drawn from the same prefix scores (a calibrated predictor)
+    dv = {}
+    for n in (8, 64, 512):
+        rng = np.random.default_rng(n)
+        sc = rng.beta(2.0, 1.2, (n, 15)).astype(np.float32)
+        s_t = torch.from_numpy(sc).to(dev)
+        tok = torch.randint(0, 150000, (n, 16), dtype=torch.int32, device=dev)
+        pos = torch.randint(0, 1 << 20, (n, 16), dtype=torch.int32, device=dev)
+        ws = svp.Workspace(256, dev)
+        holder = {}
+
+        def call():
+            holder["r"] = svp.dvl_allocate_pack(s_t, budget_per_req=8, m_cap=16 * n, tokens=tok,
+                                                positions=pos, kv_refs=tok, ws=ws)
+        us = graph_us(call)
+        r = svp.dvl_allocate_pack(s_t, budget_per_req=8, m_cap=16 * n, ws=ws)
+        q = np.minimum.accumulate(np.concatenate([np.ones((n, 1), np.float32), sc], axis=1), axis=1)
+        u = rng.random((n, 15))
+        passed = u < q[:, 1:]
+        y = np.where(passed.all(axis=1), 15, np.argmin(passed, axis=1))
+        k0 = r["k_init"].cpu().numpy().astype(np.int64)
+        k = r["k"].cpu().numpy().astype(np.int64)
+        ret = lambda kk: float(np.minimum(y, kk - 1).sum()) / max(1, int(y.sum()))
+        dv[f"n{n}"] = {"us": round(us, 2), "retention_initial": round(ret(k0), 4),
+                       "retention_adjusted": round(ret(k), 4),
+                       "mean_window_initial": round(float(k0.mean()), 2),
+                       "mean_window_adjusted": round(float(k.mean()), 2)}
+    out["dvl_allocate_pack"] = dv
+    # captured step: allocate/pack, gather, verify (full-width shapes), margin + accept
+    n_bs, V = 8, 32000
+    ctx = torch.randint(512, 8193, (n_bs,), dtype=torch.int32)
+    cu_ctx = torch.zeros(n_bs + 1, dtype=torch.int64)
+    cu_ctx[1:] = torch.cumsum(ctx.long(), 0)
+    kc = torch.randn(int(cu_ctx[-1]), 8, 128, device=dev).to(torch.bfloat16)
+    vc = torch.randn(int(cu_ctx[-1]), 8, 128, device=dev).to(torch.bfloat16)
+    pipe = VerifyPipeline(n_bs, hq=32, hkv=8, d=128, vocab=V, ctx_len=ctx.to(dev),
+                          kv_tensors=dict(k_ctx=kc, v_ctx=vc, cu_ctx=cu_ctx.to(dev)))
+    pipe.scores.copy_(torch.rand(n_bs, 15, device=dev))
+    pipe.q_full.normal_()
+    pipe.k_full.normal_()
+    pipe.v_full.normal_()
+    pipe.logits_full.normal_()
+    pipe.capture()
+    for _ in range(3):
+        pipe.step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(50):
+        pipe.step()
+    e1.record()
+    torch.cuda.synchronize()
+    out["captured_step"] = {"us": round(e0.elapsed_time(e1) / 50 * 1e3, 1),
+                            "config": "8 requests, budget 8N = 64 slots, 32q/8kv d=128, ctx U[512,8192], vocab 32000"}
+    del pipe, kc, vc
+    torch.cuda.empty_cache()
+    # stochastic verifier and draft features on the wide-head workload's logits
+    b = wl.make_batch("wide_gqa_bf16", seed=0, device=dev)
+    V = b.target_logits.shape[1]
+    ua = torch.rand(b.m_cap, device=dev)
+    un = torch.rand(b.n, device=dev)
+    wss = svp.Workspace(svp.stochastic_accept_workspace_size(b.m_cap, V), dev)
+    souts = (torch.empty(b.n, dtype=torch.int32, device=dev), torch.empty(b.n, dtype=torch.int32, device=dev),
+             torch.empty(b.m_cap, dtype=torch.float32, device=dev))
+    us = graph_us(lambda: svp.stochastic_accept(b.target_logits, b.tokens, b.cu_slots, ua, un,
+                                                temperature=1.0, ws=wss, outs=souts))
+    tb = int(b.cu_slots[-1]) * V * 2
+    out["stochastic_accept"] = {"us": round(us, 2), "logit_gbs": round(tb / (us / 1e6) / 1e9, 1),
+                                "config": "224 target rows x 248320 bf16, T = 1"}
+    wsf = svp.Workspace(svp.draft_features_workspace_size(b.draft_logits.shape[0], V), dev)
+    fout = torch.empty(b.draft_logits.shape[0], 18, dtype=torch.float32, device=dev)
+    us = graph_us(lambda: svp.draft_features(b.draft_logits, ws=wsf, out=fout))
+    db = b.draft_logits.numel() * 2
+    out["draft_features"] = {"us": round(us, 2), "logit_gbs": round(db / (us / 1e6) / 1e9, 1),
+                             "config": "192 draft rows x 248320 bf16, 18 values per row"}
+    return out
 
 
 def run_reference(args):

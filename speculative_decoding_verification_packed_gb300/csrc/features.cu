@@ -84,6 +84,44 @@ __device__ __forceinline__ void ft_acc(FtState &st, float v)
     }
 }
 
+// Fold a vector of values: one rescale to the vector maximum, then one ex2 per value
+// (ex2.approx: relative error ~2^-22, well inside the fp32 sums' own rounding).
+template <int N>
+__device__ __forceinline__ void ft_acc_vec(FtState &st, const float (&f)[N])
+{
+    constexpr float kL2e = 1.4426950408889634f;
+    float vmax = f[0];
+#pragma unroll
+    for (int h = 1; h < N; ++h)
+        vmax = fmaxf(vmax, f[h]);
+    if (vmax == -INFINITY)
+        return;
+    if (vmax > st.m) {
+        if (st.m == -INFINITY) {
+            st.s = 0.0f;
+            st.t = 0.0f;
+        } else {
+            const float d = st.m - vmax;
+            const float a = fast_exp2(d * kL2e);
+            st.t = a * (st.t + st.s * d);
+            st.s = a * st.s;
+        }
+        st.m = vmax;
+    }
+    if (vmax > st.top[kFtTop - 1]) {
+#pragma unroll
+        for (int h = 0; h < N; ++h)
+            ft_insert(st, f[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < N; ++h) {
+        const float d = fmaxf(f[h] - st.m, -1e30f);   // -inf entries: weight 0, no 0 * inf
+        const float w = fast_exp2(d * kL2e);
+        st.s += w;
+        st.t = fmaf(w, d, st.t);
+    }
+}
+
 // Merge another (m, s, t) into st.
 __device__ __forceinline__ void ft_merge_mst(FtState &st, float m2, float s2, float t2)
 {
@@ -192,20 +230,17 @@ __global__ void __launch_bounds__(kFtThreads) features_kernel(const FtParams p)
                     if (v0 + q * 32 >= nv)
                         continue;
                     const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+                    float f[VEC];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         if (DT == 1) {
-                            const float a = __uint_as_float(w[h] << 16), b = __uint_as_float(w[h] & 0xffff0000u);
-                            ft_insert(st, a);
-                            ft_insert(st, b);
-                            ft_acc(st, a);
-                            ft_acc(st, b);
+                            f[2 * h] = __uint_as_float(w[h] << 16);
+                            f[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
                         } else {
-                            const float a = __uint_as_float(w[h]);
-                            ft_insert(st, a);
-                            ft_acc(st, a);
+                            f[h] = __uint_as_float(w[h]);
                         }
                     }
+                    ft_acc_vec<VEC>(st, f);
                 }
             }
             e0 = lo + nv * VEC;

@@ -77,7 +77,54 @@ __global__ void __launch_bounds__(kStThreads1) st_rowstat_kernel(const StParams 
         const int64_t hi = lo + kStChunk < p.vocab ? lo + kStChunk : p.vocab;
         const int64_t rowb = (int64_t)r * p.row_stride;
         float m = -INFINITY, s = 0.0f;
-        for (int64_t e = lo + lane; e < hi; e += 32) {
+        // one 16-byte vector per lane per step when the rows are aligned: rescale once to
+        // the vector maximum, then one ex2 per value
+        constexpr int VEC = DT == 1 ? 8 : 4;
+        int64_t e0 = lo;
+        if (((p.row_stride * (DT == 1 ? 2 : 4)) & 15) == 0 &&
+            (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) {
+            const int64_t nv = (hi - lo) / VEC;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const uint8_t *>(p.logits) + (rowb + lo) * (DT == 1 ? 2 : 4));
+            for (int64_t v0 = lane; v0 < nv; v0 += 64) {
+                uint4 x[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    if (v0 + q * 32 < nv)
+                        x[q] = __ldg(src + v0 + q * 32);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    if (v0 + q * 32 >= nv)
+                        continue;
+                    const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+                    float f[VEC];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (DT == 1) {
+                            f[2 * h] = __uint_as_float(w[h] << 16);
+                            f[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+                        } else {
+                            f[h] = __uint_as_float(w[h]);
+                        }
+                    }
+                    float vmax = f[0];
+#pragma unroll
+                    for (int h = 1; h < VEC; ++h)
+                        vmax = fmaxf(vmax, f[h]);
+                    if (vmax > m) {
+                        s = m == -INFINITY ? 0.0f : s * fast_exp2((m - vmax) * p.c);
+                        m = vmax;
+                    }
+                    if (m != -INFINITY) {
+#pragma unroll
+                        for (int h = 0; h < VEC; ++h)
+                            s += fast_exp2((f[h] - m) * p.c);
+                    }
+                }
+            }
+            e0 = lo + nv * VEC;
+        }
+        for (int64_t e = e0 + lane; e < hi; e += 32) {
             const float v = st_load<DT>(p.logits, rowb + e);
             if (v > m) {
                 s = s * exp2f((m - v) * p.c) + 1.0f;
