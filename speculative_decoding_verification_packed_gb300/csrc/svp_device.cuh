@@ -202,8 +202,13 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 }
 
 // ---------------------------------------------------------------- tcgen05
+// The tcgen05 .sync.aligned forms below need the whole warp converged on the instruction.
+// Allocation and release come after code that only one lane of the warp ran (the MMA
+// issuer), so they reconverge the warp first; the TMEM loads and stores sit in code that
+// every lane of the warp runs in step (the same waits, warp-uniform branches).
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
+    __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      dst_smem),
                  "r"(ncols)
@@ -212,11 +217,13 @@ __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 
 __device__ __forceinline__ void tmem_relinquish()
 {
+    __syncwarp();
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
+    __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
                  "r"(ncols)
                  : "memory");

@@ -136,21 +136,35 @@ struct VtSeg {
     int64_t u_pair0;
 };
 
-// KV tiles of (request i, row block rb): context tiles of 128 keys, then candidate
+// Per-request inputs, read together (one memory round trip in the prologue).
+struct VtReq {
+    int32_t off, end, L;
+    int64_t c0;
+};
+
+__device__ __forceinline__ VtReq vt_req_load(const TcParams &p, int32_t i)
+{
+    VtReq r;
+    r.off = __ldg(p.cu_slots + i);
+    r.end = __ldg(p.cu_slots + i + 1);
+    r.L = p.ctx_len ? __ldg(p.ctx_len + i) : 0;
+    r.c0 = (!p.paged && p.cu_ctx) ? __ldg(p.cu_ctx + i) : 0;
+    return r;
+}
+
+// KV tiles of (request, row block rb): context tiles of 128 keys, then candidate
 // tiles of CB keys up to the last candidate this row block needs.
-__device__ __forceinline__ void vt_units(const TcParams &p, int32_t i, int32_t rb,
+__device__ __forceinline__ void vt_units(const TcParams &p, const VtReq &q, int32_t rb,
                                          int32_t &n_tiles, int32_t &bad)
 {
     n_tiles = 0;
     bad = 0;
-    const int32_t off = __ldg(p.cu_slots + i);
-    const int32_t end = __ldg(p.cu_slots + i + 1);
-    const int32_t k = end - off;
-    if (off < 0 || end < off || k > p.w || end > p.m_cap) {
+    const int32_t k = q.end - q.off;
+    if (q.off < 0 || q.end < q.off || k > p.w || q.end > p.m_cap) {
         bad = SVP_DEV_BAD_SLOTS;
         return;
     }
-    const int32_t L = p.ctx_len ? __ldg(p.ctx_len + i) : 0;
+    const int32_t L = q.L;
     if (L < 0) {
         bad = SVP_DEV_BAD_CONTEXT;
         return;
@@ -161,12 +175,9 @@ __device__ __forceinline__ void vt_units(const TcParams &p, int32_t i, int32_t r
                 bad = SVP_DEV_BAD_CONTEXT;
                 return;
             }
-        } else {
-            const int64_t c0 = __ldg(p.cu_ctx + i);
-            if (c0 < 0 || c0 + L > p.total_tokens) {
-                bad = SVP_DEV_BAD_CONTEXT;
-                return;
-            }
+        } else if (q.c0 < 0 || q.c0 + L > p.total_tokens) {
+            bad = SVP_DEV_BAD_CONTEXT;
+            return;
         }
     }
     const int32_t r0 = rb * p.R;
@@ -305,6 +316,66 @@ __device__ __forceinline__ RingPos ring_add(RingPos r, uint32_t n, uint32_t nslo
     return r;
 }
 
+// One merge pass over NB partial slabs staged in shared memory (ring + q * slab, row-major
+// [nact][D] fp32): acc_r = run_r + sum_q w_q[r] * slab_q[r]; the last pass scales by 1/L and
+// writes bf16 output, earlier ones keep the running sum in the first piece's slot.  Each of the
+// 128 threads owns four columns and takes eight rows at once so that the shared-memory reads of
+// all NB x 8 operands are in flight together.
+template <int NB, int D>
+__device__ __forceinline__ void vt_merge_pass(const TcParams &p, const VtRows *rs, uint32_t ring,
+                                              uint32_t slab, int32_t wq0, int32_t nact, int32_t slot0,
+                                              bool first_pass, bool last_pass, int stid)
+{
+    constexpr int C4 = D / 4;
+    constexpr int RGS = 128 / C4;
+    constexpr int RU = 8;
+    const int col4 = stid % C4, rg = stid / C4;
+    float4 *run = reinterpret_cast<float4 *>(p.part_o + (int64_t)slot0 * kRows * D) + col4;
+    uint16_t *out = reinterpret_cast<uint16_t *>(p.out) + col4 * 4;
+    const uint32_t col_b = (uint32_t)col4 * 16u;
+    for (int r0 = rg; r0 < nact; r0 += RU * RGS) {
+        float4 acc[RU];
+        int rr[RU];
+#pragma unroll
+        for (int k = 0; k < RU; ++k) {
+            rr[k] = min(r0 + k * RGS, nact - 1);   // padded lanes recompute the last row
+            acc[k] = first_pass ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldcg(run + (int64_t)rr[k] * C4);
+        }
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+            float4 x[RU];
+            float w[RU];
+#pragma unroll
+            for (int k = 0; k < RU; ++k) {
+                x[k] = ld_shared_f4(ring + q * slab + (uint32_t)rr[k] * (D * 4) + col_b);
+                w[k] = rs->wts[wq0 + q][rr[k]];
+            }
+#pragma unroll
+            for (int k = 0; k < RU; ++k) {
+                acc[k].x += w[k] * x[k].x;
+                acc[k].y += w[k] * x[k].y;
+                acc[k].z += w[k] * x[k].z;
+                acc[k].w += w[k] * x[k].w;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < RU; ++k) {
+            const int r = r0 + k * RGS;
+            if (r >= nact)
+                break;
+            if (!last_pass) {
+                __stcg(run + (int64_t)r * C4, acc[k]);
+            } else {
+                const float inv = rs->linv[r];
+                uint2 pk2;
+                pk2.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+                pk2.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+                *reinterpret_cast<uint2 *>(out + rs->orow[r]) = pk2;
+            }
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_constant__ TcParams p)
 {
@@ -399,16 +470,17 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         const int32_t q = base + tid;
         int32_t units = 0, costs = 0;
         if (q < NQ) {
+            const int32_t i = q / p.RB, rb = q - i * p.RB;
+            const VtReq rq = vt_req_load(p, i);
             int32_t nt, bad;
-            vt_units(p, q / p.RB, q % p.RB, nt, bad);
+            vt_units(p, rq, rb, nt, bad);
             bad_bits |= bad;
             units = nt * p.HG;
             costs = nt > 0 ? (nt + p.cost0) * p.HG : 0;
-            const int32_t i = q / p.RB;
-            if (q % p.RB == 0 && i < kReqCache) {
-                rs->req_off[i] = __ldg(p.cu_slots + i);
-                rs->req_len[i] = p.ctx_len ? __ldg(p.ctx_len + i) : 0;
-                rs->req_ctx[i] = (!p.paged && p.cu_ctx && p.total_tokens > 0) ? (int32_t)__ldg(p.cu_ctx + i) : 0;
+            if (rb == 0 && i < kReqCache) {
+                rs->req_off[i] = rq.off;
+                rs->req_len[i] = rq.L;
+                rs->req_ctx[i] = (p.total_tokens > 0) ? (int32_t)rq.c0 : 0;
             }
         }
         int32_t incl = units, cincl = costs;
@@ -1092,9 +1164,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 if (p.lse)
                     p.lse[rs->orow[r] / D] = (M + __log2f(Ls)) * 0.69314718055994531f;
             }
-            constexpr int C4 = D / 4;
-            constexpr int RGS = 128 / C4;
-            const int col4 = stid % C4, rg = stid / C4;
             const int32_t slot0 = rs->pslot[0];
             for (int32_t c0 = 0; c0 < np && ok; c0 += cap) {
                 const int32_t nb = min(cap, np - c0);
@@ -1115,27 +1184,23 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     break;
                 ++merge_phase;
                 const bool last_pass = c0 + cap >= np;
-                for (int r = rg; r < nact; r += RGS) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (c0 > 0)   // running sum of earlier passes, kept in the first piece's slot
-                        acc = __ldcg(reinterpret_cast<const float4 *>(p.part_o + ((int64_t)slot0 * kRows + r) * D) + col4);
-                    for (int q = 0; q < nb; ++q) {
-                        const float4 x = ld_shared_f4(sbase + p.off_ring + q * slab + (r * D + col4 * 4) * 4);
-                        const float wq = rs->wts[wq0 + q][r];
-                        acc.x += wq * x.x;
-                        acc.y += wq * x.y;
-                        acc.z += wq * x.z;
-                        acc.w += wq * x.w;
-                    }
-                    if (!last_pass) {
-                        __stcg(reinterpret_cast<float4 *>(p.part_o + ((int64_t)slot0 * kRows + r) * D) + col4, acc);
-                    } else {
-                        const float inv = rs->linv[r];
-                        uint2 pk2;
-                        pk2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-                        pk2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-                        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.out) + rs->orow[r] + col4 * 4) = pk2;
-                    }
+                const uint32_t ring = sbase + p.off_ring;
+                switch (nb) {
+#define SVP_MERGE_CASE(K)                                                                          \
+    case K:                                                                                        \
+        vt_merge_pass<K, D>(p, rs, ring, slab, wq0, nact, slot0, c0 == 0, last_pass, stid);        \
+        break;
+                    SVP_MERGE_CASE(1)
+                    SVP_MERGE_CASE(2)
+                    SVP_MERGE_CASE(3)
+                    SVP_MERGE_CASE(4)
+                    SVP_MERGE_CASE(5)
+                    SVP_MERGE_CASE(6)
+                    SVP_MERGE_CASE(7)
+                    default:
+                        vt_merge_pass<8, D>(p, rs, ring, slab, wq0, nact, slot0, c0 == 0, last_pass, stid);
+                        break;
+#undef SVP_MERGE_CASE
                 }
                 if (!last_pass)
                     __threadfence_block();
