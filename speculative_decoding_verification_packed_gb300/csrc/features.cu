@@ -6,11 +6,21 @@
 // DFlash-Mini-Lab README (DFlash7-ACT): a draft suffix is cut before the first position
 // whose top-1/top-2 margin is below a calibrated threshold (0 keeps the full block).
 //
-// Row reduction over (row, chunk of 8192 elements) units, one warp per unit: per lane a
-// sorted top-16 register list (bubble insertion, taken only by values that beat its tail)
-// and the online (max m, s = sum e^(z-m), t = sum e^(z-m) (z-m)); warp merge by 16 rounds
-// of warp max extraction; chunks of a row merged by the last warp to take the row's ticket.
-// entropy = ln s - t / s; log-sum-exp = m + ln s.  HBM-bound over rows x vocab.
+// Row reduction over (row, chunk) units, one warp per unit, the chunk sized so that the
+// units fill the GPU's resident warps once; the chunks of a row are merged by the last warp
+// to take the row's ticket.
+//  * Softmax statistics per lane: an online (max m, s = sum 2^d, t = sum 2^d d) with
+//    d = (z - m) log2 e; entropy = ln s - t ln2 / s, log-sum-exp = m + ln s.
+//  * bf16 rows: each lane streams its 16-byte vectors through a 16-slot async-copy ring in
+//    shared memory.  Top-16: each lane's 8 streams (packed word k of its 16-byte vectors, low or
+//    high half) keep their top 4 with packed bf16 min / max, branch-free; 16 rounds of warp
+//    maximum draw the chunk's top-16 from those entries.  Exact unless a stream's fourth
+//    value reaches the 16th drawn value; then (rarely) the chunk is rescanned taking only
+//    values at or above it.
+//  * Top-16, fp32 rows and the rescan: the warp's top-16 so far sorted across lanes 0..15
+//    with the 16th value as a warp-uniform threshold; a vector is offered only when its
+//    maximum beats the threshold, and an insertion is a ballot, a popcount and a lane shift.
+// HBM-bound over rows x vocab.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -18,82 +28,91 @@
 
 namespace svp {
 
-constexpr int kFtChunk = 8192;
+constexpr int kFtChunkMin = 256;    // chunk sizes are multiples of this (one 16-byte bf16 vector per lane)
+constexpr int kFtWarpsPerSm = 24;   // resident warps per SM the chunk size is planned for
+constexpr int kFtMaxChunks = 64;
 constexpr int kFtThreads = 256;
 constexpr int kFtTop = 16;
 constexpr int kFtPart = 20;   // 16 values, m, s, t, pad
+constexpr int kFtLoads = 8;   // 16-byte loads in flight per lane (fp32 / rescan path)
+constexpr int kFtStages = 16; // bf16 path: async-copy ring of 16-byte slots per lane
+constexpr int kFtSmem = (kFtThreads / 32) * kFtStages * 512;   // 64 KB per CTA
+constexpr float kFtL2e = 1.4426950408889634f;
+constexpr float kFtLn2 = 0.69314718055994531f;
+constexpr uint32_t kFtNegInf2 = 0xff80ff80u;   // packed bf16 (-inf, -inf)
+constexpr uint32_t kFtLow2 = 0xfe96fe96u;      // packed bf16 (-9.97e37, -9.97e37)
 
 struct FtParams {
     const void *logits;
     int64_t row_stride;
-    int32_t rows, vocab, chunks;
+    int32_t rows, vocab, chunks, chunk;   // chunk: elements per (row, chunk) unit
     float *feat;                // [rows, 18]
     int32_t *tickets;           // [rows]
     float *partial;             // [rows * chunks, kFtPart]
 };
 
-struct FtState {
-    float top[kFtTop];
+// Warp-distributed sorted top-16: lane j < 16 holds the j-th largest value so far
+// (-inf when fewer were seen); tau = lane 15's value, the same in every lane.
+struct FtTop {
+    float slot, tau, floor;   // floor: values at or below it are never taken
+};
+
+__device__ __forceinline__ void ft_top_init(FtTop &w)
+{
+    w.slot = -INFINITY;
+    w.tau = -INFINITY;
+    w.floor = -INFINITY;
+}
+
+// Insert v (warp-uniform, v > tau): the slots >= v are a prefix of length pos <= 15; the
+// ones after it move down one lane.
+__device__ __forceinline__ void ft_top_insert(FtTop &w, float v, int lane)
+{
+    const uint32_t ge = __ballot_sync(0xffffffffu, lane < kFtTop && w.slot >= v);
+    const int pos = __popc(ge);
+    const float prev = __shfl_up_sync(0xffffffffu, w.slot, 1);
+    if (lane < kFtTop && lane >= pos)
+        w.slot = lane == pos ? v : prev;
+    w.tau = fmaxf(__shfl_sync(0xffffffffu, w.slot, kFtTop - 1), w.floor);
+}
+
+// Offer the N values of every lane in `cand` (lanes whose vector maximum beat tau), lane by
+// lane in lane order.
+template <int N>
+__device__ __forceinline__ void ft_top_offer(FtTop &w, const float (&f)[N], uint32_t cand,
+                                             int lane)
+{
+    while (cand) {
+        const int src = __ffs(cand) - 1;
+        cand &= cand - 1;
+#pragma unroll
+        for (int h = 0; h < N; ++h) {
+            const float v = __shfl_sync(0xffffffffu, f[h], src);
+            if (v > w.tau)
+                ft_top_insert(w, v, lane);
+        }
+    }
+}
+
+// Online softmax statistics of one lane, base 2: m is the natural-unit maximum.
+struct FtStat {
     float m, s, t;
 };
 
-__device__ __forceinline__ void ft_init(FtState &st)
+__device__ __forceinline__ void ft_stat_init(FtStat &st)
 {
-#pragma unroll
-    for (int i = 0; i < kFtTop; ++i)
-        st.top[i] = -INFINITY;
     st.m = -INFINITY;
     st.s = 0.0f;
     st.t = 0.0f;
 }
 
-__device__ __forceinline__ void ft_insert(FtState &st, float v)
+// Fold N values: one rescale to the vector maximum, then one ex2 per value (ex2.approx:
+// relative error ~2^-22, well inside the fp32 sums' own rounding).  The exponent is one fma
+// against the rounded m log2 e: at T = 1 its absolute error (~1e-6 for |m| < 50) is far
+// below the sums' tolerance.  CLAMP: the values may hold -inf (weight 0, and no 0 * inf).
+template <int N, bool CLAMP>
+__device__ __forceinline__ void ft_stat_acc(FtStat &st, const float (&f)[N], float vmax)
 {
-    if (v > st.top[kFtTop - 1]) {
-        float x = v;
-#pragma unroll
-        for (int i = 0; i < kFtTop; ++i) {
-            const float hi = fmaxf(st.top[i], x);
-            x = fminf(st.top[i], x);
-            st.top[i] = hi;
-        }
-    }
-}
-
-// Fold one value into (m, s, t).
-__device__ __forceinline__ void ft_acc(FtState &st, float v)
-{
-    constexpr float kL2e = 1.4426950408889634f;
-    if (v > st.m) {
-        if (st.m == -INFINITY) {
-            st.m = v;
-            st.s = 1.0f;
-            st.t = 0.0f;
-        } else {
-            const float d = st.m - v;                  // < 0
-            const float a = exp2f(d * kL2e);
-            st.t = a * (st.t + st.s * d);
-            st.s = a * st.s + 1.0f;
-            st.m = v;
-        }
-    } else if (v != -INFINITY) {
-        const float d = v - st.m;
-        const float w = exp2f(d * kL2e);
-        st.s += w;
-        st.t += w * d;
-    }
-}
-
-// Fold a vector of values: one rescale to the vector maximum, then one ex2 per value
-// (ex2.approx: relative error ~2^-22, well inside the fp32 sums' own rounding).
-template <int N>
-__device__ __forceinline__ void ft_acc_vec(FtState &st, const float (&f)[N])
-{
-    constexpr float kL2e = 1.4426950408889634f;
-    float vmax = f[0];
-#pragma unroll
-    for (int h = 1; h < N; ++h)
-        vmax = fmaxf(vmax, f[h]);
     if (vmax == -INFINITY)
         return;
     if (vmax > st.m) {
@@ -101,31 +120,27 @@ __device__ __forceinline__ void ft_acc_vec(FtState &st, const float (&f)[N])
             st.s = 0.0f;
             st.t = 0.0f;
         } else {
-            const float d = st.m - vmax;
-            const float a = fast_exp2(d * kL2e);
-            st.t = a * (st.t + st.s * d);
+            const float d = (st.m - vmax) * kFtL2e;
+            const float a = fast_exp2(d);
+            st.t = a > 0.0f ? a * (st.t + st.s * d) : 0.0f;   // d may be huge: no 0 * inf
             st.s = a * st.s;
         }
         st.m = vmax;
     }
-    if (vmax > st.top[kFtTop - 1]) {
-#pragma unroll
-        for (int h = 0; h < N; ++h)
-            ft_insert(st, f[h]);
-    }
+    const float ml = st.m * kFtL2e;
 #pragma unroll
     for (int h = 0; h < N; ++h) {
-        const float d = fmaxf(f[h] - st.m, -1e30f);   // -inf entries: weight 0, no 0 * inf
-        const float w = fast_exp2(d * kL2e);
+        float d = fmaf(f[h], kFtL2e, -ml);
+        if (CLAMP)
+            d = fmaxf(d, -1e30f);
+        const float w = fast_exp2(d);
         st.s += w;
         st.t = fmaf(w, d, st.t);
     }
 }
 
-// Merge another (m, s, t) into st.
-__device__ __forceinline__ void ft_merge_mst(FtState &st, float m2, float s2, float t2)
+__device__ __forceinline__ void ft_stat_merge(FtStat &st, float m2, float s2, float t2)
 {
-    constexpr float kL2e = 1.4426950408889634f;
     if (m2 == -INFINITY)
         return;
     if (st.m == -INFINITY) {
@@ -135,57 +150,39 @@ __device__ __forceinline__ void ft_merge_mst(FtState &st, float m2, float s2, fl
         return;
     }
     const float M = fmaxf(st.m, m2);
-    const float d1 = st.m - M, d2 = m2 - M;
-    const float a1 = exp2f(d1 * kL2e), a2 = exp2f(d2 * kL2e);
-    st.t = a1 * (st.t + st.s * d1) + a2 * (t2 + s2 * d2);
+    const float d1 = (st.m - M) * kFtL2e, d2 = (m2 - M) * kFtL2e;
+    const float a1 = exp2f(d1), a2 = exp2f(d2);
+    st.t = (a1 > 0.0f ? a1 * (st.t + st.s * d1) : 0.0f) + (a2 > 0.0f ? a2 * (t2 + s2 * d2) : 0.0f);
     st.s = a1 * st.s + a2 * s2;
     st.m = M;
 }
 
-// Warp-wide merge: every lane ends with the warp's top-16 in out[] and the merged m, s, t.
-__device__ __forceinline__ void ft_warp_merge(FtState &st, float (&out)[kFtTop], int lane)
+__device__ __forceinline__ void ft_stat_warp(FtStat &st)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
         const float s2 = __shfl_xor_sync(0xffffffffu, st.s, o);
         const float t2 = __shfl_xor_sync(0xffffffffu, st.t, o);
-        ft_merge_mst(st, m2, s2, t2);
-    }
-#pragma unroll
-    for (int k = 0; k < kFtTop; ++k) {
-        float best = st.top[0];
-        int who = lane;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
-            const int w2 = __shfl_xor_sync(0xffffffffu, who, o);
-            if (b2 > best || (b2 == best && w2 < who)) {
-                best = b2;
-                who = w2;
-            }
-        }
-        out[k] = best;
-        if (who == lane) {
-#pragma unroll
-            for (int i = 0; i < kFtTop - 1; ++i)
-                st.top[i] = st.top[i + 1];
-            st.top[kFtTop - 1] = -INFINITY;
-        }
+        ft_stat_merge(st, m2, s2, t2);
     }
 }
 
-__device__ __forceinline__ void ft_write(const FtParams &p, int32_t r, const float (&out)[kFtTop],
-                                         float m, float s, float t)
+// Lane 0 writes the 18 features of row r (top values gathered from lanes 0..15).
+__device__ __forceinline__ void ft_write(const FtParams &p, int32_t r, const FtTop &w,
+                                         const FtStat &st, int lane)
 {
+    const float top0 = __shfl_sync(0xffffffffu, w.slot, 0);
     float *f = p.feat + (int64_t)r * 18;
-    f[0] = out[0];
-#pragma unroll
-    for (int k = 1; k < kFtTop; ++k)
-        f[k] = out[0] - out[k];
-    const float ls = logf(s);
-    f[16] = out[0] - (m + ls);
-    f[17] = ls - t / s;
+    if (lane == 0)
+        f[0] = top0;
+    else if (lane < kFtTop)
+        f[lane] = top0 - w.slot;
+    if (lane == 0) {
+        const float ls = logf(st.s);
+        f[16] = top0 - (st.m + ls);
+        f[17] = ls - st.t * kFtLn2 / st.s;
+    }
 }
 
 template <int DT>
@@ -197,96 +194,275 @@ __device__ __forceinline__ float ft_load(const void *base, int64_t idx)
 }
 
 template <int DT>
+__device__ __forceinline__ void ft_unpack(const uint4 &x, float (&f)[DT == 1 ? 8 : 4])
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        if (DT == 1) {
+            f[2 * h] = bf16_lo(w[h]);
+            f[2 * h + 1] = bf16_hi(w[h]);
+        } else {
+            f[h] = __uint_as_float(w[h]);
+        }
+    }
+}
+
+// Any dtype, any alignment: the warp-shared top-16 takes a vector only when its maximum
+// beats the threshold; WITH_STAT also folds every value into st (with -inf handling).
+template <int DT, bool WITH_STAT>
+__device__ __forceinline__ void ft_scan_generic(const FtParams &p, int64_t rowb, int64_t lo,
+                                                int64_t hi, bool vec_ok, int lane, FtTop &top,
+                                                FtStat &st)
+{
+    constexpr int VEC = DT == 1 ? 8 : 4;
+    int64_t e0 = lo;
+    if (vec_ok) {
+        const int64_t nv = (hi - lo) / VEC;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const uint8_t *>(p.logits) + (rowb + lo) * (DT == 1 ? 2 : 4));
+        for (int64_t v0 = 0; v0 < nv; v0 += kFtLoads * 32) {
+            uint4 x[kFtLoads];
+#pragma unroll
+            for (int q = 0; q < kFtLoads; ++q) {
+                const int64_t v = v0 + q * 32 + lane;
+                x[q] = v < nv ? __ldg(src + v) : make_uint4(kFtNegInf2, kFtNegInf2, kFtNegInf2, kFtNegInf2);
+            }
+#pragma unroll
+            for (int q = 0; q < kFtLoads; ++q) {
+                if (v0 + q * 32 >= nv)   // warp-uniform
+                    break;
+                float f[VEC];
+                if (v0 + q * 32 + lane < nv) {
+                    ft_unpack<DT>(x[q], f);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < VEC; ++h)
+                        f[h] = -INFINITY;
+                }
+                float vmax = f[0];
+#pragma unroll
+                for (int h = 1; h < VEC; ++h)
+                    vmax = fmaxf(vmax, f[h]);
+                if (WITH_STAT)
+                    ft_stat_acc<VEC, true>(st, f, vmax);
+                const uint32_t cand = __ballot_sync(0xffffffffu, vmax > top.tau);
+                if (cand)
+                    ft_top_offer<VEC>(top, f, cand, lane);
+            }
+        }
+        e0 = lo + nv * VEC;
+    }
+    // ragged tail (or rows without 16-byte alignment): one value per lane per step
+    for (int64_t e0b = e0; e0b < hi; e0b += 32) {
+        float f[1];
+        f[0] = e0b + lane < hi ? ft_load<DT>(p.logits, rowb + e0b + lane) : -INFINITY;
+        if (WITH_STAT)
+            ft_stat_acc<1, true>(st, f, f[0]);
+        const uint32_t cand = __ballot_sync(0xffffffffu, f[0] > top.tau);
+        if (cand)
+            ft_top_offer<1>(top, f, cand, lane);
+    }
+}
+
+// Per-stream top 4 of packed bf16 pairs (t0 >= t1 >= t2 >= t3 in each half).
+__device__ __forceinline__ void ft_top4(uint32_t &t0, uint32_t &t1, uint32_t &t2, uint32_t &t3,
+                                        uint32_t x)
+{
+    const uint32_t y1 = bf16x2_min(t0, x);
+    t0 = bf16x2_max(t0, x);
+    const uint32_t y2 = bf16x2_min(t1, y1);
+    t1 = bf16x2_max(t1, y1);
+    t3 = bf16x2_max(t3, bf16x2_min(t2, y2));
+    t2 = bf16x2_max(t2, y2);
+}
+
+__device__ __forceinline__ float ft_hmax(uint32_t w) { return fmaxf(bf16_lo(w), bf16_hi(w)); }
+
+__device__ __forceinline__ float ft_hmax4(const uint32_t (&t)[4])
+{
+    return ft_hmax(bf16x2_max(bf16x2_max(t[0], t[1]), bf16x2_max(t[2], t[3])));
+}
+
+// bf16 rows with 16-byte alignment.  Every lane has 8 streams (packed word k of its vectors,
+// low or high half); each stream keeps its top 4 with packed bf16 min / max, branch-free.
+// The chunk's top-16 is then drawn from the 1024 stream entries by 16 rounds of warp
+// maximum.  It is the exact top-16 unless some stream's fourth value reaches the 16th value
+// drawn (that stream may have dropped a fifth one above it): false is returned and the
+// caller rescans the chunk for the top-16.  The statistics see -inf as the bf16 value
+// -9.97e37 (weight 0 next to any finite maximum; the product with log2 e stays finite).
+__device__ __forceinline__ bool ft_scan_bf16(const FtParams &p, int64_t rowb, int64_t lo,
+                                             int64_t hi, int lane, uint32_t ring, FtTop &top,
+                                             FtStat &st)
+{
+    uint32_t T0[4], T1[4], T2[4], T3[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        T0[k] = T1[k] = T2[k] = T3[k] = kFtNegInf2;
+    const int64_t nv = (hi - lo) / 8;
+    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.logits) +
+                                                       (rowb + lo) * 2);
+    ring_stream<kFtStages>(ring, src, nv, lane, [&](const uint4 &x, int64_t) {
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t c[4];
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            ft_top4(T0[k], T1[k], T2[k], T3[k], w[k]);
+            c[k] = bf16x2_max(w[k], kFtLow2);
+            f[2 * k] = bf16_lo(c[k]);
+            f[2 * k + 1] = bf16_hi(c[k]);
+        }
+        ft_stat_acc<8, false>(st, f, ft_hmax4(c));
+    });
+    for (int64_t e = lo + nv * 8 + lane; e < hi; e += 32) {   // fewer than 8 values
+        const uint32_t b = __ldg(reinterpret_cast<const uint16_t *>(p.logits) + rowb + e);
+        const uint32_t w = b | 0xff800000u;                    // (value, -inf)
+        ft_top4(T0[0], T1[0], T2[0], T3[0], w);
+        float f[1];
+        f[0] = bf16_lo(bf16x2_max(w, kFtLow2));
+        ft_stat_acc<1, false>(st, f, f[0]);
+    }
+    const float fourth = ft_hmax4(T3);   // before any entry is drawn
+    float v16 = -INFINITY;
+#pragma unroll 1
+    for (int rnd = 0; rnd < kFtTop; ++rnd) {
+        const float head = ft_hmax4(T0);
+        float best = head;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+        if (lane == rnd)
+            top.slot = best;
+        v16 = best;
+        const uint32_t win = __ballot_sync(0xffffffffu, head == best);
+        if (lane == __ffs(win) - 1) {
+            // the first of this lane's streams whose head is `best` moves up one entry
+            bool done = false;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const uint32_t hm = hf ? 0xffff0000u : 0x0000ffffu;
+                    const float hv = hf ? bf16_hi(T0[k]) : bf16_lo(T0[k]);
+                    if (!done && hv == best) {
+                        T0[k] = (T0[k] & ~hm) | (T1[k] & hm);
+                        T1[k] = (T1[k] & ~hm) | (T2[k] & hm);
+                        T2[k] = (T2[k] & ~hm) | (T3[k] & hm);
+                        T3[k] = (T3[k] & ~hm) | (kFtNegInf2 & hm);
+                        done = true;
+                    }
+                }
+            }
+        }
+    }
+    top.tau = v16;
+    return __ballot_sync(0xffffffffu, fourth >= v16) == 0;
+}
+
+// Top-16 of a row from its chunks' sorted top-16 lists (kFtPart floats apart): lane l holds
+// list l of a batch of 31 (lane 31 the top-16 so far), and 16 rounds of warp maximum draw
+// the next batch top-16 (the lowest lane holding the maximum gives up its head).
+__device__ __forceinline__ void ft_merge_lists(const float *lists, int32_t nl, int lane, FtTop &top)
+{
+    for (int32_t b0 = 0; b0 < nl; b0 += 31) {
+        float l[kFtTop];
+        const int32_t q = b0 + lane;
+#pragma unroll
+        for (int k = 0; k < kFtTop; ++k) {
+            const float run = __shfl_sync(0xffffffffu, top.slot, k);
+            l[k] = lane == 31 ? run : (lane < 31 && q < nl ? __ldcg(lists + (int64_t)q * kFtPart + k) : -INFINITY);
+        }
+        float best = -INFINITY;
+#pragma unroll 1
+        for (int rnd = 0; rnd < kFtTop; ++rnd) {
+            best = l[0];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+            if (lane == rnd)
+                top.slot = best;
+            const uint32_t win = __ballot_sync(0xffffffffu, l[0] == best);
+            if (lane == __ffs(win) - 1) {
+#pragma unroll
+                for (int k = 0; k < kFtTop - 1; ++k)
+                    l[k] = l[k + 1];
+                l[kFtTop - 1] = -INFINITY;
+            }
+        }
+        top.tau = best;
+    }
+}
+
+template <int DT>
 __global__ void __launch_bounds__(kFtThreads) features_kernel(const FtParams p)
 {
+    extern __shared__ __align__(16) uint8_t ft_smem[];
     const int lane = threadIdx.x & 31;
+    const uint32_t ring = smem_u32(ft_smem) + (threadIdx.x >> 5) * (kFtStages * 512) + lane * 16;
     const int64_t warp_g = ((int64_t)blockIdx.x * kFtThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kFtThreads) >> 5;
     const int64_t units = (int64_t)p.rows * p.chunks;
-    // 16-byte vectors: 8 bf16 or 4 fp32 values
-    constexpr int VEC = DT == 1 ? 8 : 4;
     const bool vec_ok = ((p.row_stride * (DT == 1 ? 2 : 4)) & 15) == 0 &&
                         (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0;
     for (int64_t u = warp_g; u < units; u += nwarps) {
         const int32_t r = (int32_t)(u / p.chunks), ch = (int32_t)(u - (int64_t)r * p.chunks);
-        const int64_t lo = (int64_t)ch * kFtChunk;
-        const int64_t hi = lo + kFtChunk < p.vocab ? lo + kFtChunk : p.vocab;
+        const int64_t lo = (int64_t)ch * p.chunk;
+        const int64_t hi = lo + p.chunk < p.vocab ? lo + p.chunk : p.vocab;
         const int64_t rowb = (int64_t)r * p.row_stride;
-        FtState st;
-        ft_init(st);
-        int64_t e0 = lo;
-        if (vec_ok) {
-            const int64_t nv = (hi - lo) / VEC;
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                static_cast<const uint8_t *>(p.logits) + (rowb + lo) * (DT == 1 ? 2 : 4));
-            for (int64_t v0 = lane; v0 < nv; v0 += 4 * 32) {
-                uint4 x[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    x[q] = v0 + q * 32 < nv ? __ldg(src + v0 + q * 32)
-                                            : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (v0 + q * 32 >= nv)
-                        continue;
-                    const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-                    float f[VEC];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        if (DT == 1) {
-                            f[2 * h] = __uint_as_float(w[h] << 16);
-                            f[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
-                        } else {
-                            f[h] = __uint_as_float(w[h]);
-                        }
-                    }
-                    ft_acc_vec<VEC>(st, f);
-                }
+        FtTop top;
+        ft_top_init(top);
+        FtStat st;
+        ft_stat_init(st);
+        if (DT == 1 && vec_ok) {
+            if (!ft_scan_bf16(p, rowb, lo, hi, lane, ring, top, st)) {
+                // rare: rescan the chunk for its exact top-16, taking only values at or
+                // above the 16th drawn one (a lower bound of the true 16th)
+                const float v16 = top.tau;
+                ft_top_init(top);
+                if (v16 != -INFINITY)
+                    top.floor = top.tau = nextafterf(v16, -INFINITY);
+                ft_scan_generic<DT, false>(p, rowb, lo, hi, vec_ok, lane, top, st);
             }
-            e0 = lo + nv * VEC;
+        } else {
+            ft_scan_generic<DT, true>(p, rowb, lo, hi, vec_ok, lane, top, st);
         }
-        for (int64_t e = e0 + lane; e < hi; e += 32) {
-            const float a = ft_load<DT>(p.logits, rowb + e);
-            ft_insert(st, a);
-            ft_acc(st, a);
-        }
-        float out[kFtTop];
-        ft_warp_merge(st, out, lane);
+        ft_stat_warp(st);
         if (p.chunks == 1) {
-            if (lane == 0)
-                ft_write(p, r, out, st.m, st.s, st.t);
+            ft_write(p, r, top, st, lane);
             continue;
         }
         int last = 0;
-        if (lane == 0) {
+        {
             float *pp = p.partial + u * kFtPart;
-#pragma unroll
-            for (int k = 0; k < kFtTop; ++k)
-                pp[k] = out[k];
-            pp[16] = st.m;
-            pp[17] = st.s;
-            pp[18] = st.t;
-            __threadfence();
-            last = atomicAdd(p.tickets + r, 1) == p.chunks - 1;
+            if (lane < kFtTop)
+                pp[lane] = top.slot;
+            if (lane == 0) {
+                pp[16] = st.m;
+                pp[17] = st.s;
+                pp[18] = st.t;
+            }
+            __threadfence();   // every lane's partial stores before the ticket
+            __syncwarp();
+            if (lane == 0)
+                last = atomicAdd(p.tickets + r, 1) == p.chunks - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             __threadfence();
-            FtState mg;
-            ft_init(mg);
-            for (int q = lane; q < p.chunks; q += 32) {
+            FtTop mg;
+            ft_top_init(mg);
+            ft_merge_lists(p.partial + (int64_t)r * p.chunks * kFtPart, p.chunks, lane, mg);
+            FtStat ms;
+            ft_stat_init(ms);
+            for (int32_t q = lane; q < p.chunks; q += 32) {
                 const float *pp = p.partial + ((int64_t)r * p.chunks + q) * kFtPart;
-#pragma unroll
-                for (int k = 0; k < kFtTop; ++k)
-                    ft_insert(mg, __ldcg(pp + k));
-                ft_merge_mst(mg, __ldcg(pp + 16), __ldcg(pp + 17), __ldcg(pp + 18));
+                ft_stat_merge(ms, __ldcg(pp + 16), __ldcg(pp + 17), __ldcg(pp + 18));
             }
-            float fin[kFtTop];
-            ft_warp_merge(mg, fin, lane);
-            if (lane == 0) {
-                ft_write(p, r, fin, mg.m, mg.s, mg.t);
+            ft_stat_warp(ms);
+            ft_write(p, r, mg, ms, lane);
+            if (lane == 0)
                 p.tickets[r] = 0;
-            }
         }
     }
 }
@@ -307,13 +483,26 @@ __global__ void act_truncate_kernel(const float *margins, int64_t stride, int32_
     k_out[i] = k;
 }
 
-static void ft_plan(int32_t rows, int32_t vocab, int32_t &chunks, size_t &off_tk,
-                    size_t &off_part, size_t &bytes)
+// Chunk size: every row gets floor(resident warps / rows) chunks (at least one, at most
+// kFtMaxChunks), so that the units fill the resident warps at most once; chunks are
+// multiples of kFtChunkMin.
+static int32_t ft_chunk(int32_t rows, int32_t vocab, int sms)
 {
-    chunks = (vocab + kFtChunk - 1) / kFtChunk;
+    const int64_t warps = (int64_t)sms * kFtWarpsPerSm;
+    int64_t per_row = rows > 0 ? warps / rows : 1;
+    per_row = per_row < 1 ? 1 : (per_row > kFtMaxChunks ? kFtMaxChunks : per_row);
+    int64_t c = ((int64_t)vocab + per_row - 1) / per_row;
+    c = (c + kFtChunkMin - 1) / kFtChunkMin * kFtChunkMin;
+    return (int32_t)c;
+}
+
+static void ft_plan(int32_t rows, int32_t vocab, size_t &off_tk, size_t &off_part, size_t &bytes)
+{
+    const int64_t max_chunks = ((int64_t)vocab + kFtChunkMin - 1) / kFtChunkMin;
     off_tk = kWsHeader;
     off_part = (off_tk + (size_t)rows * 4 + 255) / 256 * 256;
-    bytes = off_part + (size_t)rows * chunks * kFtPart * sizeof(float);
+    bytes = off_part + (size_t)rows * (max_chunks < kFtMaxChunks ? max_chunks : kFtMaxChunks) *
+                           kFtPart * sizeof(float);
 }
 
 }  // namespace svp
@@ -324,9 +513,8 @@ extern "C" svp_status svp_draft_features_workspace_size(int32_t rows, int32_t vo
     using namespace svp;
     if (!bytes || rows < 0 || vocab < kFtTop)
         return SVP_EINVAL;
-    int32_t chunks;
     size_t a, b;
-    ft_plan(rows, vocab, chunks, a, b, *bytes);
+    ft_plan(rows, vocab, a, b, *bytes);
     return SVP_OK;
 }
 
@@ -341,7 +529,7 @@ extern "C" svp_status svp_draft_features(const void *logits, int64_t row_stride,
         return SVP_EUNSUPPORTED;
     FtParams p;
     size_t off_tk, off_part, need;
-    ft_plan(rows, vocab, p.chunks, off_tk, off_part, need);
+    ft_plan(rows, vocab, off_tk, off_part, need);
     if (ws_bytes < need)
         return SVP_EWORKSPACE;
     if (rows == 0)
@@ -358,12 +546,21 @@ extern "C" svp_status svp_draft_features(const void *logits, int64_t row_stride,
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SVP_ECUDA;
+    p.chunk = ft_chunk(rows, vocab, sms);
+    p.chunks = (vocab + p.chunk - 1) / p.chunk;
     const int64_t units = (int64_t)rows * p.chunks;
     int64_t grid = (units + (kFtThreads / 32) - 1) / (kFtThreads / 32);
-    if (grid > (int64_t)sms * 8)
-        grid = (int64_t)sms * 8;
+    if (grid > (int64_t)sms * (kFtWarpsPerSm * 32 / kFtThreads))
+        grid = (int64_t)sms * (kFtWarpsPerSm * 32 / kFtThreads);
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(features_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kFtSmem) != cudaSuccess)
+            return SVP_ECUDA;
+        configured = true;
+    }
     if (dtype == SVP_BF16)
-        features_kernel<1><<<(unsigned)grid, kFtThreads, 0, (cudaStream_t)stream>>>(p);
+        features_kernel<1><<<(unsigned)grid, kFtThreads, kFtSmem, (cudaStream_t)stream>>>(p);
     else
         features_kernel<0><<<(unsigned)grid, kFtThreads, 0, (cudaStream_t)stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;

@@ -83,25 +83,6 @@ __device__ __forceinline__ Top2 top2_warp_merge(Top2 t)
     return t;
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
-{
-    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a);
-    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162 *>(&b);
-    __nv_bfloat162 z = __hmin2(x, y);
-    return *reinterpret_cast<uint32_t *>(&z);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
-{
-    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a);
-    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162 *>(&b);
-    __nv_bfloat162 z = __hmax2(x, y);
-    return *reinterpret_cast<uint32_t *>(&z);
-}
-
 struct MarginArgs {
     const void *logits;
     int64_t row_stride;      // elements
@@ -132,15 +113,6 @@ constexpr int kMarginThreads = 256;      // 8 independent warps per CTA
 constexpr int kMarginBatch = 8;          // 16-byte loads in flight per lane (fallback path)
 constexpr int kMarginStages = 16;        // async-copy ring: 16-byte vectors in flight per lane
 constexpr int kMarginSmem = (kMarginThreads / 32) * kMarginStages * 32 * 16;   // 64 KB
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 
 // Which request owns packed row r (cu_slots non-decreasing, validated by the caller).
 __device__ __forceinline__ int32_t owner_of_row(const int32_t *cu, int32_t n, int32_t r)

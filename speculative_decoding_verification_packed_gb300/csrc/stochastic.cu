@@ -8,10 +8,15 @@
 // the unmodified P_{off_i+k_i-1} when every candidate passes.  accept_len = 1 + a,
 // next_token = the successor (inverse-CDF draw with u_next[i] in token order).
 //
-// Two launches: (1) per-row softmax statistics (max, sum of 2^((z - max) log2(e) / T)) over
-// (row, chunk) units with a per-row ticket merge, HBM-bound over the live logit rows;
-// (2) one block per request: the acceptance chain from the row statistics, then the
-// successor draw over one row (block prefix sum of per-thread chunk weights).
+// Two launches.  (1) Softmax statistics over (row, chunk) units, one warp per unit, each
+// lane streaming its 16-byte vectors through a 16-slot async-copy ring in shared memory, the chunk sized so that the units of m_cap rows
+// fill the GPU's resident warps once: the chunk's (max, sum of
+// 2^((z - max) log2(e) / T)) is kept per chunk and merged per row by the last warp to take
+// the row's ticket.  HBM-bound over the live logit rows.  (2) One block per request: warp 0
+// tests every candidate at once (probabilities from the row statistics, first rejection by
+// ballot), then walks the chunk masses of the successor row in token order to the chunk
+// that holds the draw; the block rescans only that chunk (block prefix sum of per-thread
+// masses, then one thread's elements in order).
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -20,14 +25,18 @@
 
 namespace svp {
 
-constexpr int kStChunk = 8192;          // vocabulary elements per (row, chunk) unit
+constexpr int kStChunkMin = 256;        // chunk sizes are multiples of this (one bf16 vector per lane)
+constexpr int kStWarpsPerSm = 24;       // resident pass-1 warps per SM (3 CTAs of 64 KB)
+constexpr int kStMaxChunks = 64;        // chunks per row at most
 constexpr int kStThreads1 = 256;
 constexpr int kStThreads2 = 512;
+constexpr int kStStages = 16;           // pass 1: async-copy ring of 16-byte slots per lane
+constexpr int kStSmem = (kStThreads1 / 32) * kStStages * 512;   // 64 KB per CTA
 
 struct StParams {
     const void *logits;
     int64_t row_stride;
-    int32_t m_cap, vocab, dtype, n, chunks;
+    int32_t m_cap, vocab, dtype, n, chunks, chunk;   // chunk: elements per (row, chunk) unit
     float c;                            // log2(e) / T
     const int32_t *tokens, *cu_slots;
     const float *u_accept, *u_next;
@@ -36,7 +45,7 @@ struct StParams {
     int32_t *status;
     float2 *row_stat;                   // [m_cap]: (max, sum of 2^((z - max) c))
     int32_t *tickets;                   // [m_cap]
-    float2 *partial;                    // [m_cap * chunks]
+    float2 *partial;                    // [m_cap * chunks]: the same per chunk
 };
 
 template <int DT>
@@ -62,85 +71,87 @@ __device__ __forceinline__ float2 st_merge(float2 a, float2 b, float c)
     return make_float2(a.x, a.y + b.y * exp2f((b.x - a.x) * c));
 }
 
+__device__ __forceinline__ float2 st_warp_merge(float2 a, float c)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float2 b;
+        b.x = __shfl_xor_sync(0xffffffffu, a.x, o);
+        b.y = __shfl_xor_sync(0xffffffffu, a.y, o);
+        a = st_merge(a, b, c);
+    }
+    return a;
+}
+
+// Fold N values of one lane into (m, s): one rescale to the vector maximum.
+template <int N>
+__device__ __forceinline__ void st_acc(float &m, float &s, const float (&f)[N], float c)
+{
+    float vmax = f[0];
+#pragma unroll
+    for (int h = 1; h < N; ++h)
+        vmax = fmaxf(vmax, f[h]);
+    if (vmax == -INFINITY)
+        return;
+    if (vmax > m) {
+        s = m == -INFINITY ? 0.0f : s * fast_exp2((m - vmax) * c);
+        m = vmax;
+    }
+#pragma unroll
+    for (int h = 0; h < N; ++h)
+        s += fast_exp2((f[h] - m) * c);   // the difference is exact near the max
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kStThreads1) st_rowstat_kernel(const StParams p)
 {
+    extern __shared__ __align__(16) uint8_t st_smem[];
     const int lane = threadIdx.x & 31;
+    const uint32_t ring = smem_u32(st_smem) + (threadIdx.x >> 5) * (kStStages * 512) + lane * 16;
     const int64_t warp_g = ((int64_t)blockIdx.x * kStThreads1 + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kStThreads1) >> 5;
     int32_t live = __ldg(p.cu_slots + p.n);
     live = live < 0 ? 0 : (live > p.m_cap ? p.m_cap : live);
     const int64_t units = (int64_t)live * p.chunks;
+    constexpr int VEC = DT == 1 ? 8 : 4;
+    const bool vec_ok = ((p.row_stride * (DT == 1 ? 2 : 4)) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0;
     for (int64_t u = warp_g; u < units; u += nwarps) {
         const int32_t r = (int32_t)(u / p.chunks), ch = (int32_t)(u - (int64_t)r * p.chunks);
-        const int64_t lo = (int64_t)ch * kStChunk;
-        const int64_t hi = lo + kStChunk < p.vocab ? lo + kStChunk : p.vocab;
+        const int64_t lo = (int64_t)ch * p.chunk;
+        const int64_t hi = lo + p.chunk < p.vocab ? lo + p.chunk : p.vocab;
         const int64_t rowb = (int64_t)r * p.row_stride;
         float m = -INFINITY, s = 0.0f;
-        // one 16-byte vector per lane per step when the rows are aligned: rescale once to
-        // the vector maximum, then one ex2 per value
-        constexpr int VEC = DT == 1 ? 8 : 4;
         int64_t e0 = lo;
-        if (((p.row_stride * (DT == 1 ? 2 : 4)) & 15) == 0 &&
-            (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) {
+        if (vec_ok) {
             const int64_t nv = (hi - lo) / VEC;
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 static_cast<const uint8_t *>(p.logits) + (rowb + lo) * (DT == 1 ? 2 : 4));
-            for (int64_t v0 = lane; v0 < nv; v0 += 64) {
-                uint4 x[2];
+            ring_stream<kStStages>(ring, src, nv, lane, [&](const uint4 &x, int64_t) {
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                float f[VEC];
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    if (v0 + q * 32 < nv)
-                        x[q] = __ldg(src + v0 + q * 32);
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    if (v0 + q * 32 >= nv)
-                        continue;
-                    const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-                    float f[VEC];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        if (DT == 1) {
-                            f[2 * h] = __uint_as_float(w[h] << 16);
-                            f[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
-                        } else {
-                            f[h] = __uint_as_float(w[h]);
-                        }
-                    }
-                    float vmax = f[0];
-#pragma unroll
-                    for (int h = 1; h < VEC; ++h)
-                        vmax = fmaxf(vmax, f[h]);
-                    if (vmax > m) {
-                        s = m == -INFINITY ? 0.0f : s * fast_exp2((m - vmax) * p.c);
-                        m = vmax;
-                    }
-                    if (m != -INFINITY) {
-#pragma unroll
-                        for (int h = 0; h < VEC; ++h)
-                            s += fast_exp2((f[h] - m) * p.c);
+                for (int h = 0; h < 4; ++h) {
+                    if (DT == 1) {
+                        f[2 * h] = bf16_lo(w[h]);
+                        f[2 * h + 1] = bf16_hi(w[h]);
+                    } else {
+                        f[h] = __uint_as_float(w[h]);
                     }
                 }
-            }
+                st_acc<VEC>(m, s, f, p.c);
+            });
             e0 = lo + nv * VEC;
         }
         for (int64_t e = e0 + lane; e < hi; e += 32) {
-            const float v = st_load<DT>(p.logits, rowb + e);
-            if (v > m) {
-                s = s * exp2f((m - v) * p.c) + 1.0f;
-                m = v;
-            } else {
-                s += exp2f((v - m) * p.c);
-            }
+            float f[1];
+            f[0] = st_load<DT>(p.logits, rowb + e);
+            st_acc<1>(m, s, f, p.c);
         }
-        float2 a = make_float2(m, m == -INFINITY ? 0.0f : s);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float2 b;
-            b.x = __shfl_xor_sync(0xffffffffu, a.x, o);
-            b.y = __shfl_xor_sync(0xffffffffu, a.y, o);
-            a = st_merge(a, b, p.c);
-        }
+        float2 a = st_warp_merge(make_float2(m, m == -INFINITY ? 0.0f : s), p.c);
+        // the successor draw walks the chunk masses, so every chunk's pair is kept
+        if (lane == 0)
+            p.partial[u] = a;
         if (p.chunks == 1) {
             if (lane == 0)
                 p.row_stat[r] = a;
@@ -148,7 +159,6 @@ __global__ void __launch_bounds__(kStThreads1) st_rowstat_kernel(const StParams 
         }
         int last = 0;
         if (lane == 0) {
-            p.partial[u] = a;
             __threadfence();
             last = atomicAdd(p.tickets + r, 1) == p.chunks - 1;
         }
@@ -158,13 +168,7 @@ __global__ void __launch_bounds__(kStThreads1) st_rowstat_kernel(const StParams 
             float2 t = make_float2(-INFINITY, 0.0f);
             for (int q = lane; q < p.chunks; q += 32)
                 t = st_merge(t, __ldcg(p.partial + (int64_t)r * p.chunks + q), p.c);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                float2 b;
-                b.x = __shfl_xor_sync(0xffffffffu, t.x, o);
-                b.y = __shfl_xor_sync(0xffffffffu, t.y, o);
-                t = st_merge(t, b, p.c);
-            }
+            t = st_warp_merge(t, p.c);
             if (lane == 0) {
                 p.row_stat[r] = t;
                 p.tickets[r] = 0;
@@ -176,9 +180,10 @@ __global__ void __launch_bounds__(kStThreads1) st_rowstat_kernel(const StParams 
 template <int DT>
 __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p)
 {
-    __shared__ float sh_sum[kStThreads2 / 32];
-    __shared__ float sh_total;
-    __shared__ int32_t sh_row, sh_excl, sh_claim;
+    constexpr int NW = kStThreads2 / 32;
+    __shared__ float sh_sum[NW];
+    __shared__ float sh_target, sh_m;
+    __shared__ int32_t sh_row, sh_excl, sh_chunk, sh_claim, sh_lastnz;
     const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t off = __ldg(p.cu_slots + i), end = __ldg(p.cu_slots + i + 1);
     const int32_t live = __ldg(p.cu_slots + p.n);
@@ -198,43 +203,143 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
         }
         return;
     }
-    if (tid == 0) {
-        // acceptance chain: candidate j against row off + j - 1
+    if (warp == 0) {
+        // ---- acceptance chain: lane l tests candidate j0 + l (row off + j - 1); the first
+        // rejection, found by ballot, ends the prefix.  Probabilities are written for the
+        // candidates tested in order (up to and including the first rejection).
         int32_t a = 0, excl = -1;
-        for (int32_t j = 1; j < k; ++j) {
-            const int32_t r = off + j - 1;
-            const int32_t x = __ldg(p.tokens + off + j);
-            const float2 st = p.row_stat[r];
+        for (int32_t j0 = 1; j0 < k; j0 += 32) {
+            const int32_t j = j0 + lane;
             float pr = 0.0f;
-            if (x >= 0 && x < p.vocab)
-                pr = exp2f((st_load<DT>(p.logits, (int64_t)r * p.row_stride + x) - st.x) * p.c) / st.y;
-            if (p.p_draft)
+            int32_t x = -1;
+            bool pass = true;
+            if (j < k) {
+                const int32_t r = off + j - 1;
+                x = __ldg(p.tokens + off + j);
+                const float2 st = __ldcg(p.row_stat + r);
+                if (x >= 0 && x < p.vocab)
+                    pr = exp2f((st_load<DT>(p.logits, (int64_t)r * p.row_stride + x) - st.x) * p.c) / st.y;
+                pass = __ldg(p.u_accept + off + j) < pr;
+            }
+            const uint32_t rej = __ballot_sync(0xffffffffu, !pass);
+            const int first = rej ? __ffs(rej) - 1 : 32;
+            if (p.p_draft && j < k && lane <= first)
                 p.p_draft[off + j] = pr;
-            if (__ldg(p.u_accept + off + j) < pr) {
-                ++a;
-            } else {
-                excl = x;
+            if (rej) {
+                a += first;
+                excl = __shfl_sync(0xffffffffu, x, first);
                 break;
             }
+            a += min(32, k - j0);
         }
-        p.accept_len[i] = 1 + a;
-        sh_row = off + a;
-        sh_excl = excl;
-        sh_claim = kStThreads2;
+        // ---- successor row r = off + a: chunk masses relative to the row max, the rejected
+        // token's mass taken out of its chunk; walk them in token order to the draw.
+        const int32_t r = off + a;
+        const float M = __ldcg(p.row_stat + r).x;
+        float wx = 0.0f;
+        int32_t cx = -1;
+        if (excl >= 0 && excl < p.vocab) {
+            wx = exp2f((st_load<DT>(p.logits, (int64_t)r * p.row_stride + excl) - M) * p.c);
+            cx = excl / p.chunk;
+        }
+        auto chunk_mass = [&](int32_t ch) -> float {
+            if (ch >= p.chunks)
+                return 0.0f;
+            const float2 pc = __ldcg(p.partial + (int64_t)r * p.chunks + ch);
+            float w = pc.x == -INFINITY ? 0.0f : pc.y * exp2f((pc.x - M) * p.c);
+            if (ch == cx)   // what is left within rounding of the removed token counts as none
+                w = w - wx > w * 0x1p-20f ? w - wx : 0.0f;
+            return w;
+        };
+        float tot = 0.0f;
+        for (int32_t c0 = 0; c0 < p.chunks; c0 += 32)
+            tot += chunk_mass(c0 + lane);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        const float target = __ldg(p.u_next + i) * tot;
+        int32_t sel = -1, last_nz = -1;
+        float sel_before = 0.0f, carry = 0.0f;
+        for (int32_t c0 = 0; c0 < p.chunks; c0 += 32) {
+            const float w = chunk_mass(c0 + lane);
+            float incl = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            incl += carry;
+            const float before = incl - w;
+            const uint32_t nz = __ballot_sync(0xffffffffu, w > 0.0f);
+            if (nz)
+                last_nz = c0 + 31 - __clz(nz);
+            const uint32_t hit = __ballot_sync(0xffffffffu, w > 0.0f && before <= target && target < incl);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                sel = c0 + l;
+                sel_before = __shfl_sync(0xffffffffu, before, l);
+                break;
+            }
+            carry = __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            p.accept_len[i] = 1 + a;
+            sh_row = r;
+            sh_excl = excl;
+            sh_m = M;
+            // rounding left the draw past every chunk: the last chunk with mass, whose last
+            // token with weight is taken below
+            sh_chunk = sel >= 0 ? sel : last_nz;
+            sh_target = sel >= 0 ? target - sel_before : INFINITY;
+            sh_claim = kStThreads2;
+            sh_lastnz = -1;
+        }
     }
     __syncthreads();
-    // successor: inverse-CDF draw over row sh_row without token sh_excl, in token order
-    const int32_t r = sh_row, excl = sh_excl;
-    const float m = p.row_stat[r].x;
+    const int32_t r = sh_row, excl = sh_excl, ch = sh_chunk;
+    if (ch < 0) {   // no token with weight at all (every other token underflowed)
+        if (tid == 0)
+            p.next_token[i] = -1;
+        return;
+    }
+    const float m = sh_m, target = sh_target;
     const int64_t rowb = (int64_t)r * p.row_stride;
-    const int64_t per = ((int64_t)p.vocab + kStThreads2 - 1) / kStThreads2;
-    const int64_t lo = (int64_t)tid * per;
-    const int64_t hi = lo + per < p.vocab ? lo + per : p.vocab;
+    const int64_t clo = (int64_t)ch * p.chunk;
+    const int64_t chi = clo + p.chunk < p.vocab ? clo + p.chunk : p.vocab;
+    // per thread a contiguous run of whole 16-byte vectors (the chunk starts on one)
+    constexpr int VEC = DT == 1 ? 8 : 4;
+    const int64_t per = ((chi - clo + kStThreads2 - 1) / kStThreads2 + VEC - 1) / VEC * VEC;
+    const int64_t lo = clo + (int64_t)tid * per;
+    const int64_t hi = lo + per < chi ? lo + per : chi;
+    const bool vec_ok = ((p.row_stride * (DT == 1 ? 2 : 4)) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0;
     float own = 0.0f;
-    for (int64_t e = lo; e < hi; ++e)
+    int64_t e = lo;
+    if (vec_ok) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.logits) +
+                                                           (rowb + lo) * (DT == 1 ? 2 : 4));
+        const int64_t nv = hi > lo ? (hi - lo) / VEC : 0;
+        for (int64_t v = 0; v < nv; ++v) {
+            const uint4 x = __ldg(src + v);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                if (DT == 1) {
+                    const int64_t e2 = lo + v * VEC + 2 * h;
+                    own += e2 != excl ? exp2f((bf16_lo(w[h]) - m) * p.c) : 0.0f;
+                    own += e2 + 1 != excl ? exp2f((bf16_hi(w[h]) - m) * p.c) : 0.0f;
+                } else {
+                    own += lo + v * VEC + h != excl ? exp2f((__uint_as_float(w[h]) - m) * p.c) : 0.0f;
+                }
+            }
+        }
+        e = lo + nv * VEC;
+    }
+    for (; e < hi; ++e)
         if (e != excl)
             own += exp2f((st_load<DT>(p.logits, rowb + e) - m) * p.c);
-    // block exclusive scan of the chunk weights
+    // block exclusive scan of the per-thread masses
     float incl = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -246,63 +351,70 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
         sh_sum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        float t = lane < kStThreads2 / 32 ? sh_sum[lane] : 0.0f;
+        float t = lane < NW ? sh_sum[lane] : 0.0f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, t, o);
             if (lane >= o)
                 t += y;
         }
-        if (lane < kStThreads2 / 32)
+        if (lane < NW)
             sh_sum[lane] = t;
-        if (lane == kStThreads2 / 32 - 1)
-            sh_total = t;
     }
     __syncthreads();
     const float before = (warp > 0 ? sh_sum[warp - 1] : 0.0f) + incl - own;
-    const float target = __ldg(p.u_next + i) * sh_total;
-    // the lowest chunk whose interval [before, before + own) holds the target (rounding
-    // may let two intervals touch it; the lower one is the smaller token)
-    const bool mine = own > 0.0f && before <= target &&
-                      (target < before + own || before + own >= sh_total);
-    if (mine)
+    // the lowest thread whose interval [before, before + own) holds the draw
+    if (own > 0.0f && before <= target && target < before + own)
         atomicMin(&sh_claim, tid);
+    if (own > 0.0f)
+        atomicMax(&sh_lastnz, tid);
     __syncthreads();
-    if (tid == sh_claim) {
+    const int claim = sh_claim;
+    // no claim (the draw lies past the recomputed masses by rounding): the chunk's last token
+    // with weight
+    const int who = claim < kStThreads2 ? claim : sh_lastnz;
+    if (tid == who) {
         float cum = before;
-        int32_t y = -1, last_nz = -1;
+        int32_t y = -1, lnz = -1;
         for (int64_t e = lo; e < hi; ++e) {
             if (e == excl)
                 continue;
             const float w = exp2f((st_load<DT>(p.logits, rowb + e) - m) * p.c);
             if (w > 0.0f)
-                last_nz = (int32_t)e;
+                lnz = (int32_t)e;
             cum += w;
-            if (cum > target && w > 0.0f) {
+            if (claim < kStThreads2 && cum > target && w > 0.0f) {
                 y = (int32_t)e;
                 break;
             }
         }
-        p.next_token[i] = y >= 0 ? y : last_nz;
+        p.next_token[i] = y >= 0 ? y : lnz;
     }
-    if (tid == 0 && sh_claim == kStThreads2) {
-        // rounding left the target past every chunk: the last token with weight
-        int32_t y = -1;
-        for (int64_t e = p.vocab - 1; e >= 0 && y < 0; --e)
-            if (e != excl && exp2f((st_load<DT>(p.logits, rowb + e) - m) * p.c) > 0.0f)
-                y = (int32_t)e;
-        p.next_token[i] = y;
-    }
+    if (tid == 0 && who < 0)
+        p.next_token[i] = -1;
 }
 
-static void st_plan(int32_t m_cap, int32_t vocab, int32_t &chunks, size_t &off_stat,
-                    size_t &off_tk, size_t &off_part, size_t &bytes)
+// Chunk size: the rows of m_cap get floor(resident pass-1 warps / m_cap) chunks each (at
+// least one, at most kStMaxChunks), so that the units fill the resident warps at most once;
+// chunks are multiples of kStChunkMin.
+static int32_t st_chunk(int32_t m_cap, int32_t vocab, int sms)
 {
-    chunks = (vocab + kStChunk - 1) / kStChunk;
+    const int64_t warps = (int64_t)sms * kStWarpsPerSm;
+    int64_t per_row = m_cap > 0 ? warps / m_cap : 1;
+    per_row = per_row < 1 ? 1 : (per_row > kStMaxChunks ? kStMaxChunks : per_row);
+    int64_t c = ((int64_t)vocab + per_row - 1) / per_row;
+    c = (c + kStChunkMin - 1) / kStChunkMin * kStChunkMin;
+    return (int32_t)c;
+}
+
+static void st_plan(int32_t m_cap, int32_t vocab, size_t &off_stat, size_t &off_tk,
+                    size_t &off_part, size_t &bytes)
+{
+    const int64_t mc = ((int64_t)vocab + kStChunkMin - 1) / kStChunkMin;
     off_stat = kWsHeader;
     off_tk = off_stat + (size_t)m_cap * sizeof(float2);
     off_part = (off_tk + (size_t)m_cap * 4 + 255) / 256 * 256;
-    bytes = off_part + (size_t)m_cap * chunks * sizeof(float2);
+    bytes = off_part + (size_t)m_cap * (mc < kStMaxChunks ? mc : kStMaxChunks) * sizeof(float2);
 }
 
 }  // namespace svp
@@ -313,9 +425,8 @@ extern "C" svp_status svp_stochastic_accept_workspace_size(int32_t m_cap, int32_
     using namespace svp;
     if (!bytes || m_cap < 0 || vocab < 2)
         return SVP_EINVAL;
-    int32_t chunks;
     size_t a, b, c;
-    st_plan(m_cap, vocab, chunks, a, b, c, *bytes);
+    st_plan(m_cap, vocab, a, b, c, *bytes);
     return SVP_OK;
 }
 
@@ -337,7 +448,7 @@ extern "C" svp_status svp_stochastic_accept(const void *logits, int64_t row_stri
         return SVP_EUNSUPPORTED;
     StParams p;
     size_t off_stat, off_tk, off_part, need;
-    st_plan(m_cap, vocab, p.chunks, off_stat, off_tk, off_part, need);
+    st_plan(m_cap, vocab, off_stat, off_tk, off_part, need);
     if (ws_bytes < need)
         return SVP_EWORKSPACE;
     if (n == 0)
@@ -365,18 +476,29 @@ extern "C" svp_status svp_stochastic_accept(const void *logits, int64_t row_stri
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SVP_ECUDA;
+    p.chunk = st_chunk(m_cap, vocab, sms);
+    p.chunks = (vocab + p.chunk - 1) / p.chunk;
     const int64_t units = (int64_t)m_cap * p.chunks;
     int64_t grid1 = (units + (kStThreads1 / 32) - 1) / (kStThreads1 / 32);
-    if (grid1 > (int64_t)sms * 8)
-        grid1 = (int64_t)sms * 8;
+    if (grid1 > (int64_t)sms * (kStWarpsPerSm * 32 / kStThreads1))
+        grid1 = (int64_t)sms * (kStWarpsPerSm * 32 / kStThreads1);
     if (grid1 < 1)
         grid1 = 1;
     cudaStream_t s = (cudaStream_t)stream;
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(st_rowstat_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(st_rowstat_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStSmem) != cudaSuccess)
+            return SVP_ECUDA;
+        configured = true;
+    }
     if (dtype == SVP_BF16) {
-        st_rowstat_kernel<1><<<(unsigned)grid1, kStThreads1, 0, s>>>(p);
+        st_rowstat_kernel<1><<<(unsigned)grid1, kStThreads1, kStSmem, s>>>(p);
         st_accept_kernel<1><<<n, kStThreads2, 0, s>>>(p);
     } else {
-        st_rowstat_kernel<0><<<(unsigned)grid1, kStThreads1, 0, s>>>(p);
+        st_rowstat_kernel<0><<<(unsigned)grid1, kStThreads1, kStSmem, s>>>(p);
         st_accept_kernel<0><<<n, kStThreads2, 0, s>>>(p);
     }
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;

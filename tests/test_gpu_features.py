@@ -50,3 +50,31 @@ def test_act_truncation():
         assert k.cpu().tolist() == expect.tolist()
         assert k1.cpu().tolist() == expect.tolist()
     assert svp.act_truncate(margins, n=n, w=w, threshold=0.0).cpu().tolist() == [w] * n
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_features_adversarial_layouts(dtype):
+    """Rows whose top values share one lane position (every 256th element, so a kernel that
+    keeps a few values per lane stream must notice and recover), a row of equal values, a
+    row with -inf entries and fewer than 16 finite values, and a row whose top-16 sits in
+    one contiguous run."""
+    V = 20000
+    g = torch.Generator().manual_seed(9)
+    z = torch.randn(5, V, generator=g) * 2.0
+    idx = 5 + 256 * torch.arange(20)
+    z[0, idx] = 20.0 + torch.arange(20, dtype=torch.float32) * 0.25
+    z[1] = 1.5
+    z[2] = -float("inf")
+    z[2, torch.tensor([3, 700, 9000, 19999])] = torch.tensor([1.0, 4.0, -2.0, 0.5])
+    z[3, 1000:1016] = 30.0 - torch.arange(16, dtype=torch.float32)
+    z[4, idx[:6]] = 25.0
+    z = z.to(dtype)
+    ref = ft.draft_features(z.float().numpy().astype(np.float64))
+    out = svp.draft_features(z.cuda()).cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref[:, 1:16])
+    assert out[:, 0].tolist() == ref[:, 0].tolist()
+    assert np.array_equal(np.isfinite(out[:, 1:16]), fin)
+    d = np.abs(np.where(fin, out[:, 1:16], 0.0) - np.where(fin, ref[:, 1:16], 0.0))
+    assert np.all(d <= 6e-8 * np.maximum(np.abs(np.where(fin, ref[:, 1:16], 0.0)), np.abs(ref[:, :1])))
+    assert np.abs(out[:, 16] - ref[:, 16]).max() <= 1e-4
+    assert np.abs(out[:, 17] - ref[:, 17]).max() <= 1e-4 * np.log(V)
