@@ -11,8 +11,7 @@
 // to take the row's ticket.
 //  * Softmax statistics per lane: an online (max m, s = sum 2^d, t = sum 2^d d) with
 //    d = (z - m) log2 e; entropy = ln s - t ln2 / s, log-sum-exp = m + ln s.
-//  * bf16 rows: each lane streams its 16-byte vectors through a 16-slot async-copy ring in
-//    shared memory.  Top-16: each lane's 8 streams (packed word k of its 16-byte vectors, low or
+//  * Top-16, bf16 rows: each lane's 8 streams (packed word k of its 16-byte vectors, low or
 //    high half) keep their top 4 with packed bf16 min / max, branch-free; 16 rounds of warp
 //    maximum draw the chunk's top-16 from those entries.  Exact unless a stream's fourth
 //    value reaches the 16th drawn value; then (rarely) the chunk is rescanned taking only
@@ -34,9 +33,7 @@ constexpr int kFtMaxChunks = 64;
 constexpr int kFtThreads = 256;
 constexpr int kFtTop = 16;
 constexpr int kFtPart = 20;   // 16 values, m, s, t, pad
-constexpr int kFtLoads = 8;   // 16-byte loads in flight per lane (fp32 / rescan path)
-constexpr int kFtStages = 16; // bf16 path: async-copy ring of 16-byte slots per lane
-constexpr int kFtSmem = (kFtThreads / 32) * kFtStages * 512;   // 64 KB per CTA
+constexpr int kFtLoads = 8;   // 16-byte loads in flight per lane
 constexpr float kFtL2e = 1.4426950408889634f;
 constexpr float kFtLn2 = 0.69314718055994531f;
 constexpr uint32_t kFtNegInf2 = 0xff80ff80u;   // packed bf16 (-inf, -inf)
@@ -292,8 +289,7 @@ __device__ __forceinline__ float ft_hmax4(const uint32_t (&t)[4])
 // caller rescans the chunk for the top-16.  The statistics see -inf as the bf16 value
 // -9.97e37 (weight 0 next to any finite maximum; the product with log2 e stays finite).
 __device__ __forceinline__ bool ft_scan_bf16(const FtParams &p, int64_t rowb, int64_t lo,
-                                             int64_t hi, int lane, uint32_t ring, FtTop &top,
-                                             FtStat &st)
+                                             int64_t hi, int lane, FtTop &top, FtStat &st)
 {
     uint32_t T0[4], T1[4], T2[4], T3[4];
 #pragma unroll
@@ -302,19 +298,30 @@ __device__ __forceinline__ bool ft_scan_bf16(const FtParams &p, int64_t rowb, in
     const int64_t nv = (hi - lo) / 8;
     const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.logits) +
                                                        (rowb + lo) * 2);
-    ring_stream<kFtStages>(ring, src, nv, lane, [&](const uint4 &x, int64_t) {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t c[4];
-        float f[8];
+    for (int64_t v0 = 0; v0 < nv; v0 += kFtLoads * 32) {
+        uint4 x[kFtLoads];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            ft_top4(T0[k], T1[k], T2[k], T3[k], w[k]);
-            c[k] = bf16x2_max(w[k], kFtLow2);
-            f[2 * k] = bf16_lo(c[k]);
-            f[2 * k + 1] = bf16_hi(c[k]);
+        for (int q = 0; q < kFtLoads; ++q) {
+            const int64_t v = v0 + q * 32 + lane;
+            x[q] = v < nv ? __ldg(src + v) : make_uint4(kFtNegInf2, kFtNegInf2, kFtNegInf2, kFtNegInf2);
         }
-        ft_stat_acc<8, false>(st, f, ft_hmax4(c));
-    });
+#pragma unroll
+        for (int q = 0; q < kFtLoads; ++q) {
+            if (v0 + q * 32 + lane >= nv)
+                continue;
+            const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+            uint32_t c[4];
+            float f[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                ft_top4(T0[k], T1[k], T2[k], T3[k], w[k]);
+                c[k] = bf16x2_max(w[k], kFtLow2);
+                f[2 * k] = bf16_lo(c[k]);
+                f[2 * k + 1] = bf16_hi(c[k]);
+            }
+            ft_stat_acc<8, false>(st, f, ft_hmax4(c));
+        }
+    }
     for (int64_t e = lo + nv * 8 + lane; e < hi; e += 32) {   // fewer than 8 values
         const uint32_t b = __ldg(reinterpret_cast<const uint16_t *>(p.logits) + rowb + e);
         const uint32_t w = b | 0xff800000u;                    // (value, -inf)
@@ -397,9 +404,7 @@ __device__ __forceinline__ void ft_merge_lists(const float *lists, int32_t nl, i
 template <int DT>
 __global__ void __launch_bounds__(kFtThreads) features_kernel(const FtParams p)
 {
-    extern __shared__ __align__(16) uint8_t ft_smem[];
     const int lane = threadIdx.x & 31;
-    const uint32_t ring = smem_u32(ft_smem) + (threadIdx.x >> 5) * (kFtStages * 512) + lane * 16;
     const int64_t warp_g = ((int64_t)blockIdx.x * kFtThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kFtThreads) >> 5;
     const int64_t units = (int64_t)p.rows * p.chunks;
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(kFtThreads) features_kernel(const FtParams p)
         FtStat st;
         ft_stat_init(st);
         if (DT == 1 && vec_ok) {
-            if (!ft_scan_bf16(p, rowb, lo, hi, lane, ring, top, st)) {
+            if (!ft_scan_bf16(p, rowb, lo, hi, lane, top, st)) {
                 // rare: rescan the chunk for its exact top-16, taking only values at or
                 // above the 16th drawn one (a lower bound of the true 16th)
                 const float v16 = top.tau;
@@ -552,15 +557,8 @@ extern "C" svp_status svp_draft_features(const void *logits, int64_t row_stride,
     int64_t grid = (units + (kFtThreads / 32) - 1) / (kFtThreads / 32);
     if (grid > (int64_t)sms * (kFtWarpsPerSm * 32 / kFtThreads))
         grid = (int64_t)sms * (kFtWarpsPerSm * 32 / kFtThreads);
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(features_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kFtSmem) != cudaSuccess)
-            return SVP_ECUDA;
-        configured = true;
-    }
     if (dtype == SVP_BF16)
-        features_kernel<1><<<(unsigned)grid, kFtThreads, kFtSmem, (cudaStream_t)stream>>>(p);
+        features_kernel<1><<<(unsigned)grid, kFtThreads, 0, (cudaStream_t)stream>>>(p);
     else
         features_kernel<0><<<(unsigned)grid, kFtThreads, 0, (cudaStream_t)stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;

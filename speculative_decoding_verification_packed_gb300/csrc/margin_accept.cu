@@ -363,13 +363,20 @@ struct MarginPlan {
     size_t off_row_ticket, off_row_argmax, off_req_ticket, off_partial, bytes;
 };
 
+int sm_count();   // defined in api.cu
+
+// Chunks per row: at least enough for units of at most 16384 elements (32 KB of bf16), and
+// as many as fill the resident warps once (3 CTAs of 8 warps per SM, bounded by the ring's
+// shared memory), so that every warp gets one unit of about the same size; at most 64.
 static MarginPlan margin_plan(int32_t rows, int32_t vocab, int32_t n)
 {
     MarginPlan p{};
-    const int32_t target = 16384;  // elements per unit (32 KB of bf16), one warp each
-    p.chunks_per_row = (vocab + target - 1) / target;
-    if (p.chunks_per_row < 1)
-        p.chunks_per_row = 1;
+    const int32_t target = 16384;
+    const int64_t warps = (int64_t)sm_count() * 3 * (kMarginThreads / 32);
+    int64_t per_row = (vocab + target - 1) / target;
+    const int64_t fill = rows > 0 ? warps / rows : 1;
+    per_row = per_row > fill ? per_row : (fill > 64 ? 64 : fill);
+    p.chunks_per_row = per_row < 1 ? 1 : (int32_t)per_row;
     int32_t c = (vocab + p.chunks_per_row - 1) / p.chunks_per_row;
     c = (c + 7) / 8 * 8;
     p.chunk = c;
@@ -383,8 +390,6 @@ static MarginPlan margin_plan(int32_t rows, int32_t vocab, int32_t n)
     p.bytes = o;
     return p;
 }
-
-int sm_count();   // defined in api.cu
 
 svp_status margin_workspace(int32_t rows, int32_t vocab, int32_t n, size_t *bytes)
 {

@@ -883,13 +883,18 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 uint32_t pk[4][16];
                 float ymax = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 4; c += 2) {
                     if (c < nch) {
-                        uint32_t sr[32];
-                        tmem_ld32(sa + c * 32, sr);
+                        uint32_t sr0[32], sr1[32];
+                        tmem_ld32(sa + c * 32, sr0);
+                        if (c + 1 < nch)
+                            tmem_ld32(sa + (c + 1) * 32, sr1);
                         tmem_wait_ld();
-                        vt_chunk(sr, mref_a + c * 128, jr_a + c * 128, key_ok, !is_ctx, cbase + t,
+                        vt_chunk(sr0, mref_a + c * 128, jr_a + c * 128, key_ok, !is_ctx, cbase + t,
                                  cl2, pk[c], ymax);
+                        if (c + 1 < nch)
+                            vt_chunk(sr1, mref_a + (c + 1) * 128, jr_a + (c + 1) * 128, key_ok, !is_ctx,
+                                     cbase + t, cl2, pk[c + 1], ymax);
                     }
                 }
                 const bool hit = ymax > kSlack;
