@@ -1126,7 +1126,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             // the first pass's slabs are on their way while the row statistics are formed
             auto issue_pass = [&](int32_t c0) {
                 const int32_t nb = min(cap, np - c0);
-                asm volatile("fence.proxy.async;" ::: "memory");
+                asm volatile("fence.proxy.async.global;" ::: "memory");
                 mbar_arrive_expect_tx(bar_merge, (uint32_t)nb * slab);
                 for (int q = 0; q < nb; ++q)
                     bulk_g2s(sbase + p.off_ring + q * slab,
