@@ -313,8 +313,10 @@ svp_status svp_stochastic_accept_workspace_size(int32_t m_cap, int32_t vocab, si
  * cu_slots [n+1]; u_accept [m_cap] fp32 and u_next [n] fp32, uniform draws in [0, 1)
  * supplied by the caller; outputs accept_len [n], next_token [n] int32 and p_draft [m_cap]
  * (the acceptance probability of each tested candidate; may be NULL).  Rows >=
- * cu_slots[n] are not read.  Invalid cu_slots set SVP_DEV_BAD_SLOTS; the request gets
- * accept_len 0 and next_token -1.
+ * cu_slots[n] are not read.  Invalid cu_slots (cu_slots[0] != 0, a decrease, or
+ * cu_slots[n] > m_cap) set SVP_DEV_BAD_SLOTS: no row is read and every request gets
+ * accept_len 0 and next_token -1.  ws zeroed once (svp_workspace_init); the kernel leaves
+ * its tickets at zero.
  */
 svp_status svp_stochastic_accept(const void *logits, int64_t row_stride, int32_t m_cap,
                                  int32_t vocab, svp_dtype dtype, const int32_t *tokens,

@@ -110,8 +110,21 @@ __global__ void __launch_bounds__(kStThreads1) st_rowstat_kernel(const StParams 
     const uint32_t ring = smem_u32(st_smem) + (threadIdx.x >> 5) * (kStStages * 512) + lane * 16;
     const int64_t warp_g = ((int64_t)blockIdx.x * kStThreads1 + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kStThreads1) >> 5;
+    // cu_slots must start at 0, never decrease and end within m_cap; otherwise no row is read
+    // and the second pass gives every request 0 / -1
+    bool bad = (lane == 0) && (__ldg(p.cu_slots) != 0);
+    for (int32_t i = lane; i < p.n; i += 32)
+        bad |= __ldg(p.cu_slots + i + 1) < __ldg(p.cu_slots + i);
     int32_t live = __ldg(p.cu_slots + p.n);
-    live = live < 0 ? 0 : (live > p.m_cap ? p.m_cap : live);
+    bad |= live > p.m_cap || live < 0;
+    const bool valid = !__any_sync(0xffffffffu, bad);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        p.status[2] = valid ? 0 : 1;
+        if (!valid)
+            set_status(p.status, SVP_DEV_BAD_SLOTS);
+    }
+    if (!valid)
+        live = 0;
     const int64_t units = (int64_t)live * p.chunks;
     constexpr int VEC = DT == 1 ? 8 : 4;
     const bool vec_ok = ((p.row_stride * (DT == 1 ? 2 : 4)) & 15) == 0 &&
@@ -186,10 +199,10 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
     __shared__ int32_t sh_row, sh_excl, sh_chunk, sh_claim, sh_lastnz;
     const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t off = __ldg(p.cu_slots + i), end = __ldg(p.cu_slots + i + 1);
-    const int32_t live = __ldg(p.cu_slots + p.n);
-    if (off < 0 || end < off || end > p.m_cap || live > p.m_cap) {
+    // the first pass found cu_slots invalid (it set the status bit): nothing was read
+    if (*reinterpret_cast<volatile int32_t *>(p.status + 2) != 0 || off < 0 || end < off ||
+        end > p.m_cap) {
         if (tid == 0) {
-            set_status(p.status, SVP_DEV_BAD_SLOTS);
             p.accept_len[i] = 0;
             p.next_token[i] = -1;
         }

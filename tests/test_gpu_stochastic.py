@@ -115,3 +115,24 @@ def test_output_law_of_replicated_requests():
             chi2 += (counts.get(key, 0) - e) ** 2 / e
             dof += 1
     assert chi2 < (dof - 1) + 4 * np.sqrt(2 * (dof - 1)) + 10, (chi2, dof)
+
+
+def test_invalid_slots_set_status_and_empty_results():
+    """A decreasing cu_slots is rejected on the device: status bit, every request 0 / -1, and
+    the workspace stays usable (a valid call right after agrees with the reference)."""
+    n, V = 4, 3000
+    z, zf, tok, cu, ua, un = _batch(21, n, V, torch.bfloat16, kmax=6)
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    ws = svp.Workspace(svp.stochastic_accept_workspace_size(z.shape[0], V))
+    bad = cu.copy()
+    bad[1] = bad[2] + 1            # cu_slots[1] > cu_slots[2]: a decrease
+    acc, nxt, _ = svp.stochastic_accept(z.cuda(), d(tok), d(bad), d(ua), d(un), temperature=1.0, ws=ws)
+    assert ws.read_status() != 0
+    assert acc.cpu().tolist() == [0] * n and nxt.cpu().tolist() == [-1] * n
+    acc, nxt, _ = svp.stochastic_accept(z.cuda(), d(tok), d(cu), d(ua), d(un), temperature=1.0, ws=ws)
+    ref_acc, ref_nxt, _ = st.stochastic_accept(zf, tok, cu, 1.0, ua.astype(np.float64), un.astype(np.float64))
+    assert ws.read_status() == 0
+    a, y = acc.cpu().numpy(), nxt.cpu().numpy()
+    for i in range(n):
+        if not _borderline(zf, tok, cu, 1.0, ua, un, i, int(y[i])):
+            assert (a[i], y[i]) == (ref_acc[i], ref_nxt[i])
