@@ -7,7 +7,8 @@
 // supplies the successor).
 //
 // Design (HBM-bound stream, no tensor cores):
-//   * Each logits row is cut into equal chunks of <= 8192 elements; every warp is an
+//   * Each logits row is cut into equal chunks of <= 16384 elements, more of them when the
+//     batch is short, so that the units fill the resident warps once; every warp is an
 //     independent worker on one (row, chunk) unit at a time (no CTA barriers).
 //   * Each lane keeps a (top1, top1_idx, top2) triple over 16-byte vector loads, eight
 //     in flight at once, updated without branches (a skip test on the lane's own top-2
@@ -110,9 +111,7 @@ struct MarginArgs {
 };
 
 constexpr int kMarginThreads = 256;      // 8 independent warps per CTA
-constexpr int kMarginBatch = 8;          // 16-byte loads in flight per lane (fallback path)
-constexpr int kMarginStages = 16;        // async-copy ring: 16-byte vectors in flight per lane
-constexpr int kMarginSmem = (kMarginThreads / 32) * kMarginStages * 32 * 16;   // 64 KB
+constexpr int kMarginBatch = 8;          // 16-byte loads in flight per lane
 
 // Which request owns packed row r (cu_slots non-decreasing, validated by the caller).
 __device__ __forceinline__ int32_t owner_of_row(const int32_t *cu, int32_t n, int32_t r)
@@ -139,7 +138,7 @@ __device__ __forceinline__ float load_elem(const MarginArgs &a, int64_t row, int
 // One warp scans elements [c0, c1) of a row; lane-local triples, indices increasing.
 template <bool kBf16>
 __device__ __forceinline__ Top2 scan_chunk_warp(const MarginArgs &a, int64_t row, int32_t c0,
-                                                int32_t c1, int lane, uint8_t *ring_base)
+                                                int32_t c1, int lane)
 {
     Top2 t = top2_identity();
     constexpr int VW = kBf16 ? 8 : 4;        // elements per 16-byte vector
@@ -156,38 +155,32 @@ __device__ __forceinline__ Top2 scan_chunk_warp(const MarginArgs &a, int64_t row
             uint32_t p1 = 0xff80ff80u, p2 = 0xff80ff80u;
             float vmax = -INFINITY;
             int32_t pos = -1;
-            // each lane streams its own vectors v = lane, lane + 32, ... through a ring of
-            // kMarginStages 16-byte slots (cp.async; every lane reads only what it copied)
-            const uint32_t ring = smem_u32(ring_base) + lane * 16;
-            for (int st = 0; st < kMarginStages; ++st) {
-                const int32_t v = st * 32 + lane;
-                if (v < nvec)
-                    cp_async16(ring + st * 512, vp + v);
-                cp_async_commit();
-            }
-            for (int32_t k = 0; k * 32 + lane < nvec; ++k) {
-                cp_async_wait<kMarginStages - 1>();
-                const int32_t v = k * 32 + lane;
-                const uint32_t slot = ring + (k % kMarginStages) * 512;
-                const int4 x = ld_shared_i4(slot);
-                const uint32_t w[4] = {(uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w};
+            // each lane loads its own vectors v = lane, lane + 32, ..., eight in flight
+            for (int32_t v0 = 0; v0 < nvec; v0 += 32 * kMarginBatch) {
+                uint4 buf[kMarginBatch];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    p2 = bf16x2_max(p2, bf16x2_min(p1, w[h]));
-                    p1 = bf16x2_max(p1, w[h]);
+                for (int u = 0; u < kMarginBatch; ++u) {
+                    const int32_t v = v0 + u * 32 + lane;
+                    buf[u] = (v < nvec) ? __ldcs(vp + v) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
                 }
-                const uint32_t m4 = bf16x2_max(bf16x2_max(w[0], w[1]), bf16x2_max(w[2], w[3]));
-                const float m8 = fmaxf(bf16_lo(m4), bf16_hi(m4));
-                const bool take = m8 > vmax || pos < 0;
-                pos = take ? v : pos;
-                vmax = take ? fmaxf(vmax, m8) : vmax;
-                // the slot is refilled only after its value has been consumed
-                const int32_t vn = v + kMarginStages * 32;
-                if (vn < nvec)
-                    cp_async16(slot, vp + vn);
-                cp_async_commit();
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int32_t v = v0 + u * 32 + lane;
+                    if (v >= nvec)
+                        break;
+                    const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        p2 = bf16x2_max(p2, bf16x2_min(p1, w[h]));
+                        p1 = bf16x2_max(p1, w[h]);
+                    }
+                    const uint32_t m4 = bf16x2_max(bf16x2_max(w[0], w[1]), bf16x2_max(w[2], w[3]));
+                    const float m8 = fmaxf(bf16_lo(m4), bf16_hi(m4));
+                    const bool take = m8 > vmax || pos < 0;
+                    pos = take ? v : pos;
+                    vmax = take ? fmaxf(vmax, m8) : vmax;
+                }
             }
-            cp_async_wait<0>();
             if (pos >= 0) {
                 const float a1 = bf16_lo(p1), b1 = bf16_hi(p1);
                 t.v1 = fmaxf(a1, b1);
@@ -244,11 +237,9 @@ __device__ void finish_request(const MarginArgs &a, int32_t i)
 }
 
 template <bool kBf16>
-__global__ void __launch_bounds__(kMarginThreads) margin_kernel(MarginArgs a)
+__global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
 {
-    extern __shared__ __align__(16) uint8_t margin_smem[];
     const int lane = threadIdx.x & 31;
-    uint8_t *ring_base = margin_smem + (threadIdx.x >> 5) * (kMarginStages * 512);
     const int64_t gwarp = ((int64_t)blockIdx.x * kMarginThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kMarginThreads) >> 5;
 
@@ -275,7 +266,7 @@ __global__ void __launch_bounds__(kMarginThreads) margin_kernel(MarginArgs a)
         const int32_t ch = (int32_t)(w % a.chunks_per_row);
         const int32_t c0 = ch * a.chunk;
         const int32_t c1 = min(a.vocab, c0 + a.chunk);
-        Top2 t = top2_warp_merge(scan_chunk_warp<kBf16>(a, row, c0, c1, lane, ring_base));
+        Top2 t = top2_warp_merge(scan_chunk_warp<kBf16>(a, row, c0, c1, lane));
         int last = 0;
         if (lane == 0) {
             a.partial[row * a.chunks_per_row + ch] = t;
@@ -366,13 +357,13 @@ struct MarginPlan {
 int sm_count();   // defined in api.cu
 
 // Chunks per row: at least enough for units of at most 16384 elements (32 KB of bf16), and
-// as many as fill the resident warps once (3 CTAs of 8 warps per SM, bounded by the ring's
-// shared memory), so that every warp gets one unit of about the same size; at most 64.
+// as many as fill the resident warps once (4 CTAs of 8 warps per SM at 64 registers), so
+// that every warp gets one unit of about the same size; at most 64.
 static MarginPlan margin_plan(int32_t rows, int32_t vocab, int32_t n)
 {
     MarginPlan p{};
     const int32_t target = 16384;
-    const int64_t warps = (int64_t)sm_count() * 3 * (kMarginThreads / 32);
+    const int64_t warps = (int64_t)sm_count() * 4 * (kMarginThreads / 32);
     int64_t per_row = (vocab + target - 1) / target;
     const int64_t fill = rows > 0 ? warps / rows : 1;
     per_row = per_row > fill ? per_row : (fill > 64 ? 64 : fill);
@@ -451,19 +442,10 @@ svp_status margin_launch(const void *logits, int64_t row_stride, int32_t rows, i
         grid = (int64_t)sm_count() * 8;
     if (grid < 1)
         grid = 1;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(margin_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMarginSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(margin_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMarginSmem) != cudaSuccess)
-            return SVP_ECUDA;
-        configured = true;
-    }
     if (dtype == SVP_BF16)
-        margin_kernel<true><<<(unsigned)grid, kMarginThreads, kMarginSmem, stream>>>(a);
+        margin_kernel<true><<<(unsigned)grid, kMarginThreads, 0, stream>>>(a);
     else
-        margin_kernel<false><<<(unsigned)grid, kMarginThreads, kMarginSmem, stream>>>(a);
+        margin_kernel<false><<<(unsigned)grid, kMarginThreads, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
 }
 
