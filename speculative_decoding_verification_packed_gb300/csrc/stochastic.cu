@@ -8,8 +8,8 @@
 // the unmodified P_{off_i+k_i-1} when every candidate passes.  accept_len = 1 + a,
 // next_token = the successor (inverse-CDF draw with u_next[i] in token order).
 //
-// Two launches.  (1) Softmax statistics over (row, chunk) units, one warp per unit, each
-// lane streaming its 16-byte vectors through a 16-slot async-copy ring in shared memory, the chunk sized so that the units of m_cap rows
+// Two launches.  (1) Softmax statistics over (row, chunk) units, one warp per unit with
+// eight 16-byte loads in flight per lane, the chunk sized so that the units of m_cap rows
 // fill the GPU's resident warps once: the chunk's (max, sum of
 // 2^((z - max) log2(e) / T)) is kept per chunk and merged per row by the last warp to take
 // the row's ticket.  HBM-bound over the live logit rows.  (2) One block per request: warp 0
@@ -26,12 +26,11 @@
 namespace svp {
 
 constexpr int kStChunkMin = 256;        // chunk sizes are multiples of this (one bf16 vector per lane)
-constexpr int kStWarpsPerSm = 24;       // resident pass-1 warps per SM (3 CTAs of 64 KB)
+constexpr int kStWarpsPerSm = 32;       // resident pass-1 warps per SM (4 CTAs of 8 warps at 64 registers)
 constexpr int kStMaxChunks = 64;        // chunks per row at most
 constexpr int kStThreads1 = 256;
 constexpr int kStThreads2 = 512;
-constexpr int kStStages = 16;           // pass 1: async-copy ring of 16-byte slots per lane
-constexpr int kStSmem = (kStThreads1 / 32) * kStStages * 512;   // 64 KB per CTA
+constexpr int kStLoads = 8;             // pass 1: 16-byte loads in flight per lane
 
 struct StParams {
     const void *logits;
@@ -103,11 +102,9 @@ __device__ __forceinline__ void st_acc(float &m, float &s, const float (&f)[N], 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kStThreads1) st_rowstat_kernel(const StParams p)
+__global__ void __launch_bounds__(kStThreads1, 4) st_rowstat_kernel(const StParams p)
 {
-    extern __shared__ __align__(16) uint8_t st_smem[];
     const int lane = threadIdx.x & 31;
-    const uint32_t ring = smem_u32(st_smem) + (threadIdx.x >> 5) * (kStStages * 512) + lane * 16;
     const int64_t warp_g = ((int64_t)blockIdx.x * kStThreads1 + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kStThreads1) >> 5;
     // cu_slots must start at 0, never decrease and end within m_cap; otherwise no row is read
@@ -140,20 +137,31 @@ __global__ void __launch_bounds__(kStThreads1) st_rowstat_kernel(const StParams 
             const int64_t nv = (hi - lo) / VEC;
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 static_cast<const uint8_t *>(p.logits) + (rowb + lo) * (DT == 1 ? 2 : 4));
-            ring_stream<kStStages>(ring, src, nv, lane, [&](const uint4 &x, int64_t) {
-                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-                float f[VEC];
+            for (int64_t v0 = 0; v0 < nv; v0 += kStLoads * 32) {
+                uint4 x[kStLoads];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    if (DT == 1) {
-                        f[2 * h] = bf16_lo(w[h]);
-                        f[2 * h + 1] = bf16_hi(w[h]);
-                    } else {
-                        f[h] = __uint_as_float(w[h]);
-                    }
+                for (int q = 0; q < kStLoads; ++q) {
+                    const int64_t v = v0 + q * 32 + lane;
+                    x[q] = v < nv ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
                 }
-                st_acc<VEC>(m, s, f, p.c);
-            });
+#pragma unroll
+                for (int q = 0; q < kStLoads; ++q) {
+                    if (v0 + q * 32 + lane >= nv)
+                        continue;
+                    const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+                    float f[VEC];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (DT == 1) {
+                            f[2 * h] = bf16_lo(w[h]);
+                            f[2 * h + 1] = bf16_hi(w[h]);
+                        } else {
+                            f[h] = __uint_as_float(w[h]);
+                        }
+                    }
+                    st_acc<VEC>(m, s, f, p.c);
+                }
+            }
             e0 = lo + nv * VEC;
         }
         for (int64_t e = e0 + lane; e < hi; e += 32) {
@@ -498,20 +506,11 @@ extern "C" svp_status svp_stochastic_accept(const void *logits, int64_t row_stri
     if (grid1 < 1)
         grid1 = 1;
     cudaStream_t s = (cudaStream_t)stream;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(st_rowstat_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kStSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(st_rowstat_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kStSmem) != cudaSuccess)
-            return SVP_ECUDA;
-        configured = true;
-    }
     if (dtype == SVP_BF16) {
-        st_rowstat_kernel<1><<<(unsigned)grid1, kStThreads1, kStSmem, s>>>(p);
+        st_rowstat_kernel<1><<<(unsigned)grid1, kStThreads1, 0, s>>>(p);
         st_accept_kernel<1><<<n, kStThreads2, 0, s>>>(p);
     } else {
-        st_rowstat_kernel<0><<<(unsigned)grid1, kStThreads1, kStSmem, s>>>(p);
+        st_rowstat_kernel<0><<<(unsigned)grid1, kStThreads1, 0, s>>>(p);
         st_accept_kernel<0><<<n, kStThreads2, 0, s>>>(p);
     }
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
