@@ -364,48 +364,6 @@ __device__ __forceinline__ int4 ld_shared_i4(uint32_t addr)
     return v;
 }
 
-// 16-byte global -> shared copies in the async-copy groups of the issuing thread.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Streams the 16-byte vectors v = lane, lane + 32, ... (v < nv) of src through this lane's
-// ring of S shared-memory slots 512 bytes apart (`ring` = the lane's slot 0): S copies in
-// flight, each slot refilled only after its vector was handed to f(x, v).  Every lane reads
-// back only what it copied, so no barrier is needed; f runs per lane (the lanes' trip counts
-// differ at the tail), so it must not hold warp-collective operations.
-template <int S, typename F>
-__device__ __forceinline__ void ring_stream(uint32_t ring, const uint4 *src, int64_t nv, int lane,
-                                            F &&f)
-{
-#pragma unroll
-    for (int st = 0; st < S; ++st) {
-        const int64_t v = (int64_t)st * 32 + lane;
-        if (v < nv)
-            cp_async16(ring + st * 512, src + v);
-        cp_async_commit();
-    }
-    for (int64_t k = 0; k * 32 + lane < nv; ++k) {
-        cp_async_wait<S - 1>();
-        const int64_t v = k * 32 + lane;
-        const uint32_t slot = ring + (uint32_t)(k % S) * 512u;
-        uint4 x;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
-                     : "r"(slot));
-        f(x, v);
-        const int64_t vn = v + (int64_t)S * 32;
-        if (vn < nv)
-            cp_async16(slot, src + vn);
-        cp_async_commit();
-    }
-    cp_async_wait<0>();
-}
-
 // The low / high bf16 of a packed pair, widened to fp32 (exact).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
