@@ -686,10 +686,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                                       ad + (uint64_t)((ks >> 2) * (kSubBytes >> 4) + (ks & 3) * 2),
                                       bd + (uint64_t)((ks >> 2) * qsub16 + (ks & 3) * 2), idesc_s,
                                       (h | ks) ? 1u : 0u);
+                        // this half's slot is free once its MMAs are done
+                        tc_commit(bar_empty(ring_add(kpos, (uint32_t)h, (uint32_t)nslot).slot));
                     }
                     tc_commit(bar_sfull(b));
-                    for (int h = 0; h < DH; ++h)
-                        tc_commit(bar_empty(ring_add(kpos, (uint32_t)h, (uint32_t)nslot).slot));
                     if (k == nt - 1)
                         tc_commit(bar_qempty);   // Q no longer read by this segment
                     kpos = ring_add(kpos, 2u * DH, (uint32_t)nslot);
@@ -777,14 +777,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                             if (ks < k16)   // 16 keys (2048 bytes) per MMA
                                 tc_mma_ss(tmem + TM_O + h * NR, av + (uint64_t)(ks * 128),
                                           bp + (uint64_t)(ks * 128), idesc_o, ks ? 1u : acc0);
+                        // this half's V slot is free once its MMAs are done
+                        tc_commit(bar_empty(ring_add(ppos, (uint32_t)(DH + h), (uint32_t)nslot).slot));
                     }
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
                         if (ks < k16)
                             tc_mma_ss(tmem + TM_L, ao, bp + (uint64_t)(ks * 128), idesc_l, ks ? 1u : acc0);
                     tc_commit(bar_pvdone(pb));
-                    for (int h = 0; h < DH; ++h)
-                        tc_commit(bar_empty(ring_add(ppos, (uint32_t)(DH + h), (uint32_t)nslot).slot));
                     ppos = ring_add(ppos, 2u * DH, (uint32_t)nslot);
                 }
                 ++nseg;
