@@ -529,12 +529,14 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def graph_us(fn, reps: int = 100) -> float:
+def graph_us(fn, reps: int = 100, inner: int = 1) -> float:
     """Device time of one call (CUDA-graph replay, events on the replay stream).  fn may be a
     list of calls on different inputs (rotated so that consecutive calls do not find their
-    input in L2); the time is per call."""
+    input in L2); the time is per call.  inner > 1 captures the calls that many times in one
+    graph, so that a call shorter than the host's replay overhead is still timed on the
+    device."""
     import torch
-    fns = list(fn) if isinstance(fn, (list, tuple)) else [fn]
+    fns = (list(fn) if isinstance(fn, (list, tuple)) else [fn]) * inner
     for _ in range(3):
         for f in fns:
             f()
@@ -583,7 +585,7 @@ def next_rows_extras(svp, dev):
         def call():
             holder["r"] = svp.dvl_allocate_pack(s_t, budget_per_req=8, m_cap=16 * n, tokens=tok,
                                                 positions=pos, kv_refs=tok, ws=ws)
-        us = graph_us(call)
+        us = graph_us(call, inner=20)
         r = svp.dvl_allocate_pack(s_t, budget_per_req=8, m_cap=16 * n, ws=ws)
         q = np.minimum.accumulate(np.concatenate([np.ones((n, 1), np.float32), sc], axis=1), axis=1)
         u = rng.random((n, 15))

@@ -23,6 +23,7 @@ namespace svp {
 constexpr int kDvlThreads = 1024;
 constexpr int kDvlMaxRequests = 2048;
 constexpr int kDvlMaxW = 16;
+constexpr int kDvlRow = kDvlMaxW + 1;   // row stride of the score table: one request per bank step
 
 struct DvlParams {
     const float *scores;        // [n_bs, w-1]
@@ -51,7 +52,8 @@ struct DvlShared {
     int32_t hist[256];
     int32_t warp_tot[32];
     int32_t bcast[4];
-    float q[kDvlMaxRequests * kDvlMaxW];   // prefix scores, row stride kDvlMaxW
+    float q[kDvlMaxRequests * kDvlRow];    // prefix scores, row stride kDvlRow (no bank conflicts
+                                           // when threads walk one request each)
 };
 
 // Sum over the block (every thread gets the result).
@@ -120,7 +122,7 @@ __device__ void dvl_select(DvlShared &sh, int n_live, int w, bool grow, int32_t 
     auto lo = [&](int i) { return grow ? sh.k0[i] : 1; };
     auto hi = [&](int i) { return grow ? w : sh.k0[i]; };
     auto key = [&](int i, int j) {
-        const uint32_t k = dvl_key(sh.q[i * kDvlMaxW + j]);
+        const uint32_t k = dvl_key(sh.q[i * kDvlRow + j]);
         return grow ? k : ~k;                   // selection of the largest keys
     };
     uint32_t prefix = 0, mask = 0;
@@ -129,12 +131,33 @@ __device__ void dvl_select(DvlShared &sh, int n_live, int w, bool grow, int32_t 
         for (int b = tid; b < 256; b += blockDim.x)
             sh.hist[b] = 0;
         __syncthreads();
-        for (int i = tid; i < n_live; i += blockDim.x)
-            for (int j = lo(i); j < hi(i); ++j) {
+        if (n_live * w > 2 * (int)blockDim.x) {
+            // many requests: one request per thread
+            for (int i = tid; i < n_live; i += blockDim.x)
+                for (int j = lo(i); j < hi(i); ++j) {
+                    const uint32_t k = key(i, j);
+                    if ((k & mask) == prefix)
+                        atomicAdd(&sh.hist[(k >> shift) & 255u], 1);
+                }
+        } else
+        // few requests: one (request, slot) pair per thread, and lanes that hit the same
+        // bucket add together (keys crowd into a few buckets; same-address atomics serialise)
+        for (int c = tid; c < n_live * w; c += blockDim.x) {
+            const int i = c / w, j = c - i * w;
+            bool hit = false;
+            uint32_t bucket = 0;
+            if (j >= lo(i) && j < hi(i)) {
                 const uint32_t k = key(i, j);
-                if ((k & mask) == prefix)
-                    atomicAdd(&sh.hist[(k >> shift) & 255u], 1);
+                hit = (k & mask) == prefix;
+                bucket = (k >> shift) & 255u;
             }
+            const uint32_t act = __ballot_sync(__activemask(), hit);
+            if (hit) {
+                const uint32_t peers = __match_any_sync(act, bucket);
+                if ((tid & 31) == __ffs(peers) - 1)
+                    atomicAdd(&sh.hist[bucket], __popc(peers));
+            }
+        }
         __syncthreads();
         if (tid < 32) {
             // lane L owns buckets 255-8L .. 248-8L, scanned from the top
@@ -213,13 +236,19 @@ __global__ void __launch_bounds__(kDvlThreads, 1) dvl_kernel(const DvlParams p)
     }
     const int32_t budget = bad ? 0 : (int32_t)budget64;
 
+    // the scores, staged with coalesced loads (one memory round trip, not w - 1 of them)
+    for (int e = tid; e < n_bs * (w - 1); e += blockDim.x) {
+        const int i = e / (w - 1), j = e - i * (w - 1) + 1;
+        sh.q[i * kDvlRow + j] = __ldg(p.scores + e);
+    }
+    __syncthreads();
     // prefix scores (cumulative minimum after the anchor's 1) and initial lengths
     for (int i = tid; i < n_bs; i += blockDim.x) {
         float qv = 1.0f, acc = 0.0f;
-        sh.q[i * kDvlMaxW] = 1.0f;
+        sh.q[i * kDvlRow] = 1.0f;
         for (int j = 1; j < w; ++j) {
-            qv = fminf(qv, __ldg(p.scores + (int64_t)i * (w - 1) + (j - 1)));
-            sh.q[i * kDvlMaxW + j] = qv;
+            qv = fminf(qv, sh.q[i * kDvlRow + j]);
+            sh.q[i * kDvlRow + j] = qv;
             acc = __fadd_rn(acc, qv);
         }
         int32_t k0 = 0;
