@@ -22,7 +22,7 @@ step by step in the page's order:
 7. packing: row offset_i + j of every field takes field[i, j] for j < k_i; rows past the
    live slots hold the field's placeholder.
 
-Readings where the page is silent (each is stated in the design doc): the score sum and the
+Readings where the page is silent: the score sum and the
 rounding are done in fp32 (the kernel's precision, because they decide integers), adding
 positions 1..W-1 in order; rounding is to nearest, ties to even; ties between requests go
 to the lowest request index, both when growing and when shrinking; the budget is
