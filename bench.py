@@ -491,6 +491,8 @@ def run_ours(args):
                                               (opl["draft_margin"] / 1e3) / 1e9, 1)
                 e["margin_accept_gbs"] = round(int(osets[0].cu_slots[-1]) * V * 2 /
                                                (opl["margin_accept"] / 1e3) / 1e9, 1)
+                e["draft_margin_frac"] = round(e["draft_margin_gbs"] / hbm_peak, 4)
+                e["margin_accept_frac"] = round(e["margin_accept_gbs"] / hbm_peak, 4)
             extras[other] = e
             del osets
             torch.cuda.empty_cache()
@@ -516,6 +518,10 @@ def run_ours(args):
                                          "tflops": round(flops / (pms / 1e3) / 1e12, 1),
                                          "frac_of_bf16_peak": round(flops / (pms / 1e3) / 1e12 / tf_peak, 4)}
         extras.update(next_rows_extras(svp, dev))
+        # logit-stream kernels against the same measured HBM copy peak
+        for key in ("stochastic_accept", "draft_features"):
+            if key in extras:
+                extras[key]["logit_frac"] = round(extras[key]["logit_gbs"] / hbm_peak, 4)
         result["extras"] = extras
 
     if not args.no_cpu_baseline and rank == 0 and world == 1:

@@ -78,3 +78,22 @@ def test_features_adversarial_layouts(dtype):
     assert np.all(d <= 6e-8 * np.maximum(np.abs(np.where(fin, ref[:, 1:16], 0.0)), np.abs(ref[:, :1])))
     assert np.abs(out[:, 16] - ref[:, 16]).max() <= 1e-4
     assert np.abs(out[:, 17] - ref[:, 17]).max() <= 1e-4 * np.log(V)
+
+
+def test_full_size_wide_gqa_sampled_rows():
+    """The launch the bench times: 192 draft rows x 248,320 bf16; sampled rows against the
+    oracle."""
+    from speculative_decoding_verification_packed_gb300 import workloads as wl
+    b = wl.make_batch("wide_gqa_bf16", seed=0, device="cuda")
+    z = b.draft_logits
+    rows, V = z.shape
+    ws = svp.Workspace(svp.draft_features_workspace_size(rows, V))
+    out = svp.draft_features(z, ws=ws).cpu().numpy().astype(np.float64)
+    pick = [0, 1, 63, 64, 127, 150, rows - 1]
+    ref = ft.draft_features(z[pick].float().cpu().numpy().astype(np.float64))
+    o = out[pick]
+    assert o[:, 0].tolist() == ref[:, 0].tolist()
+    assert np.all(np.abs(o[:, 1:16] - ref[:, 1:16]) <= 6e-8 * np.maximum(np.abs(ref[:, 1:16]), np.abs(ref[:, :1])))
+    assert np.abs(o[:, 16] - ref[:, 16]).max() <= 1e-4
+    assert np.abs(o[:, 17] - ref[:, 17]).max() <= 1e-4 * np.log(V)
+    assert np.all(np.isfinite(out))

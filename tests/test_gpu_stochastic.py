@@ -136,3 +136,34 @@ def test_invalid_slots_set_status_and_empty_results():
     for i in range(n):
         if not _borderline(zf, tok, cu, 1.0, ua, un, i, int(y[i])):
             assert (a[i], y[i]) == (ref_acc[i], ref_nxt[i])
+
+
+def test_full_size_wide_gqa_sampled_requests():
+    """The launch the bench times: 224 target rows x 248,320 bf16 (32 requests of 7 slots),
+    T = 1; sampled requests against the oracle run on their own rows."""
+    from speculative_decoding_verification_packed_gb300 import workloads as wl
+    b = wl.make_batch("wide_gqa_bf16", seed=0, device="cuda")
+    V = b.target_logits.shape[1]
+    rng = np.random.default_rng(21)
+    ua = rng.random(b.m_cap).astype(np.float32)
+    un = rng.random(b.n).astype(np.float32)
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    ws = svp.Workspace(svp.stochastic_accept_workspace_size(b.m_cap, V))
+    acc, nxt, pd = svp.stochastic_accept(b.target_logits, b.tokens, b.cu_slots, d(ua), d(un),
+                                         temperature=1.0, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0
+    acc, nxt, pd = acc.cpu().numpy(), nxt.cpu().numpy(), pd.cpu().numpy()
+    cu = b.cu_slots.cpu().numpy()
+    tok = b.tokens.cpu().numpy()
+    for i in (0, 5, 13, 22, 31):
+        lo, hi = int(cu[i]), int(cu[i + 1])
+        zf = b.target_logits[lo:hi].float().cpu().numpy().astype(np.float64)
+        cu1 = np.array([0, hi - lo], dtype=np.int32)
+        o_acc, o_nxt, o_pd = st.stochastic_accept(zf, tok[lo:hi], cu1, 1.0, ua[lo:hi].astype(np.float64),
+                                                  un[i:i + 1].astype(np.float64))
+        tested = ~np.isnan(o_pd) & ~np.isnan(pd[lo:hi])
+        assert np.abs(pd[lo:hi][tested] - o_pd[tested]).max(initial=0.0) <= TOL
+        if acc[i] != o_acc[0] or nxt[i] != o_nxt[0]:
+            assert _borderline(zf, tok[lo:hi], cu1, 1.0, ua[lo:hi], un[i:i + 1], 0, int(nxt[i])), \
+                (i, acc[i], o_acc[0], nxt[i], o_nxt[0])
