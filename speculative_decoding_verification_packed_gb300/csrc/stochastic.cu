@@ -30,6 +30,7 @@ constexpr int kStWarpsPerSm = 32;       // resident pass-1 warps per SM (4 CTAs 
 constexpr int kStMaxChunks = 64;        // chunks per row at most
 constexpr int kStThreads1 = 256;
 constexpr int kStThreads2 = 512;
+constexpr int kStPrefRows = 16;        // rows of a request whose chunk statistics pass 2 prefetches
 constexpr int kStLoads = 8;             // pass 1: 16-byte loads in flight per lane
 
 struct StParams {
@@ -202,6 +203,7 @@ template <int DT>
 __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p)
 {
     constexpr int NW = kStThreads2 / 32;
+    __shared__ float2 sh_part[kStPrefRows * kStMaxChunks];   // chunk statistics of the first rows
     __shared__ float sh_sum[NW];
     __shared__ float sh_target, sh_m;
     __shared__ int32_t sh_row, sh_excl, sh_chunk, sh_claim, sh_lastnz;
@@ -224,22 +226,37 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
         }
         return;
     }
+    // the other warps bring the chunk statistics of the request's first rows (any of them
+    // may be the successor row) into shared memory while warp 0 runs the acceptance chain
+    const int32_t npre = k < kStPrefRows ? k : kStPrefRows;
+    if (warp > 0) {
+        for (int32_t x = tid - 32; x < npre * p.chunks; x += kStThreads2 - 32)
+            sh_part[x] = __ldcg(p.partial + (int64_t)off * p.chunks + x);
+        named_bar_arrive(1, kStThreads2);
+    }
     if (warp == 0) {
         // ---- acceptance chain: lane l tests candidate j0 + l (row off + j - 1); the first
         // rejection, found by ballot, ends the prefix.  Probabilities are written for the
         // candidates tested in order (up to and including the first rejection).
+        // the last row's maximum, in case every candidate is accepted
+        const float m_last = lane == 0 ? __ldcg(p.row_stat + off + k - 1).x : 0.0f;
         int32_t a = 0, excl = -1;
+        float M = 0.0f, zx = -INFINITY;   // successor row maximum; rejected token's logit
+        bool rejected = false;
         for (int32_t j0 = 1; j0 < k; j0 += 32) {
             const int32_t j = j0 + lane;
-            float pr = 0.0f;
+            float pr = 0.0f, z = -INFINITY, mr = 0.0f;
             int32_t x = -1;
             bool pass = true;
             if (j < k) {
                 const int32_t r = off + j - 1;
                 x = __ldg(p.tokens + off + j);
                 const float2 st = __ldcg(p.row_stat + r);
-                if (x >= 0 && x < p.vocab)
-                    pr = exp2f((st_load<DT>(p.logits, (int64_t)r * p.row_stride + x) - st.x) * p.c) / st.y;
+                mr = st.x;
+                if (x >= 0 && x < p.vocab) {
+                    z = st_load<DT>(p.logits, (int64_t)r * p.row_stride + x);
+                    pr = exp2f((z - st.x) * p.c) / st.y;
+                }
                 pass = __ldg(p.u_accept + off + j) < pr;
             }
             const uint32_t rej = __ballot_sync(0xffffffffu, !pass);
@@ -247,26 +264,33 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
             if (p.p_draft && j < k && lane <= first)
                 p.p_draft[off + j] = pr;
             if (rej) {
+                // the successor row is the row the rejected candidate was tested on
                 a += first;
                 excl = __shfl_sync(0xffffffffu, x, first);
+                zx = __shfl_sync(0xffffffffu, z, first);
+                M = __shfl_sync(0xffffffffu, mr, first);
+                rejected = true;
                 break;
             }
             a += min(32, k - j0);
         }
+        if (!rejected)
+            M = __shfl_sync(0xffffffffu, m_last, 0);
         // ---- successor row r = off + a: chunk masses relative to the row max, the rejected
         // token's mass taken out of its chunk; walk them in token order to the draw.
         const int32_t r = off + a;
-        const float M = __ldcg(p.row_stat + r).x;
         float wx = 0.0f;
         int32_t cx = -1;
         if (excl >= 0 && excl < p.vocab) {
-            wx = exp2f((st_load<DT>(p.logits, (int64_t)r * p.row_stride + excl) - M) * p.c);
+            wx = exp2f((zx - M) * p.c);
             cx = excl / p.chunk;
         }
+        named_bar_sync(1, kStThreads2);   // the prefetched chunk statistics are in
+        const float2 *prow = a < npre ? sh_part + a * p.chunks : p.partial + (int64_t)r * p.chunks;
         auto chunk_mass = [&](int32_t ch) -> float {
             if (ch >= p.chunks)
                 return 0.0f;
-            const float2 pc = __ldcg(p.partial + (int64_t)r * p.chunks + ch);
+            const float2 pc = a < npre ? prow[ch] : __ldcg(prow + ch);
             float w = pc.x == -INFINITY ? 0.0f : pc.y * exp2f((pc.x - M) * p.c);
             if (ch == cx)   // what is left within rounding of the removed token counts as none
                 w = w - wx > w * 0x1p-20f ? w - wx : 0.0f;
