@@ -83,9 +83,12 @@ __device__ __forceinline__ float2 st_warp_merge(float2 a, float c)
     return a;
 }
 
-// Fold N values of one lane into (m, s): one rescale to the vector maximum.
+// Fold N values of one lane into (m, s): one rescale to the vector maximum.  The exponent
+// of each value is one fma against mc = m c rounded to fp32: the rounding shifts every
+// exponent of this lane's (m, s) by the same amount (|m c| 2^-24), a common factor of the
+// chunk's weights that is far below the probabilities' tolerance.
 template <int N>
-__device__ __forceinline__ void st_acc(float &m, float &s, const float (&f)[N], float c)
+__device__ __forceinline__ void st_acc(float &m, float &mc, float &s, const float (&f)[N], float c)
 {
     float vmax = f[0];
 #pragma unroll
@@ -96,10 +99,11 @@ __device__ __forceinline__ void st_acc(float &m, float &s, const float (&f)[N], 
     if (vmax > m) {
         s = m == -INFINITY ? 0.0f : s * fast_exp2((m - vmax) * c);
         m = vmax;
+        mc = m * c;
     }
 #pragma unroll
     for (int h = 0; h < N; ++h)
-        s += fast_exp2((f[h] - m) * c);   // the difference is exact near the max
+        s += fast_exp2(fmaf(f[h], c, -mc));
 }
 
 template <int DT>
@@ -132,7 +136,7 @@ __global__ void __launch_bounds__(kStThreads1, 4) st_rowstat_kernel(const StPara
         const int64_t lo = (int64_t)ch * p.chunk;
         const int64_t hi = lo + p.chunk < p.vocab ? lo + p.chunk : p.vocab;
         const int64_t rowb = (int64_t)r * p.row_stride;
-        float m = -INFINITY, s = 0.0f;
+        float m = -INFINITY, mc = 0.0f, s = 0.0f;
         int64_t e0 = lo;
         if (vec_ok) {
             const int64_t nv = (hi - lo) / VEC;
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(kStThreads1, 4) st_rowstat_kernel(const StPara
                             f[h] = __uint_as_float(w[h]);
                         }
                     }
-                    st_acc<VEC>(m, s, f, p.c);
+                    st_acc<VEC>(m, mc, s, f, p.c);
                 }
             }
             e0 = lo + nv * VEC;
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(kStThreads1, 4) st_rowstat_kernel(const StPara
         for (int64_t e = e0 + lane; e < hi; e += 32) {
             float f[1];
             f[0] = st_load<DT>(p.logits, rowb + e);
-            st_acc<1>(m, s, f, p.c);
+            st_acc<1>(m, mc, s, f, p.c);
         }
         float2 a = st_warp_merge(make_float2(m, m == -INFINITY ? 0.0f : s), p.c);
         // the successor draw walks the chunk masses, so every chunk's pair is kept
