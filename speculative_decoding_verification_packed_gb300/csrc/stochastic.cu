@@ -30,6 +30,7 @@ constexpr int kStWarpsPerSm = 32;       // resident pass-1 warps per SM (4 CTAs 
 constexpr int kStMaxChunks = 64;        // chunks per row at most
 constexpr int kStThreads1 = 256;
 constexpr int kStThreads2 = 512;
+constexpr uint32_t kStNegInf2 = 0xff80ff80u;   // packed bf16 (-inf, -inf)
 constexpr int kStPrefRows = 16;        // rows of a request whose chunk statistics pass 2 prefetches
 constexpr int kStLoads = 8;             // pass 1: 16-byte loads in flight per lane
 
@@ -147,24 +148,46 @@ __global__ void __launch_bounds__(kStThreads1, 4) st_rowstat_kernel(const StPara
 #pragma unroll
                 for (int q = 0; q < kStLoads; ++q) {
                     const int64_t v = v0 + q * 32 + lane;
-                    x[q] = v < nv ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+                    x[q] = v < nv ? __ldg(src + v) : make_uint4(kStNegInf2, kStNegInf2, kStNegInf2, kStNegInf2);
                 }
+                if constexpr (DT == 1) {
+                    // bf16: the batch maximum by packed max (vectors past the end hold -inf),
+                    // one rescale, then every value of the batch
+                    uint32_t b2 = kStNegInf2;
 #pragma unroll
-                for (int q = 0; q < kStLoads; ++q) {
-                    if (v0 + q * 32 + lane >= nv)
+                    for (int q = 0; q < kStLoads; ++q)
+                        b2 = bf16x2_max(bf16x2_max(b2, bf16x2_max(x[q].x, x[q].y)), bf16x2_max(x[q].z, x[q].w));
+                    const float bmax = fmaxf(bf16_lo(b2), bf16_hi(b2));
+                    if (bmax == -INFINITY)
                         continue;
-                    const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-                    float f[VEC];
+                    if (bmax > m) {
+                        s = m == -INFINITY ? 0.0f : s * fast_exp2((m - bmax) * p.c);
+                        m = bmax;
+                        mc = m * p.c;
+                    }
+                    float s0 = 0.0f, s1 = 0.0f;   // two chains of adds
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        if (DT == 1) {
-                            f[2 * h] = bf16_lo(w[h]);
-                            f[2 * h + 1] = bf16_hi(w[h]);
-                        } else {
-                            f[h] = __uint_as_float(w[h]);
+                    for (int q = 0; q < kStLoads; ++q) {
+                        const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            s0 += fast_exp2(fmaf(bf16_lo(w[h]), p.c, -mc));
+                            s1 += fast_exp2(fmaf(bf16_hi(w[h]), p.c, -mc));
                         }
                     }
-                    st_acc<VEC>(m, mc, s, f, p.c);
+                    s += s0 + s1;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < kStLoads; ++q) {
+                        if (v0 + q * 32 + lane >= nv)
+                            continue;
+                        float f[VEC];
+                        f[0] = __uint_as_float(x[q].x);
+                        f[1] = __uint_as_float(x[q].y);
+                        f[2] = __uint_as_float(x[q].z);
+                        f[3] = __uint_as_float(x[q].w);
+                        st_acc<VEC>(m, mc, s, f, p.c);
+                    }
                 }
             }
             e0 = lo + nv * VEC;
