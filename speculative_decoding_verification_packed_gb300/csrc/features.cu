@@ -107,11 +107,9 @@ __device__ __forceinline__ void ft_stat_init(FtStat &st)
 // relative error ~2^-22, well inside the fp32 sums' own rounding).  The exponent is one fma
 // against the rounded m log2 e: at T = 1 its absolute error (~1e-6 for |m| < 50) is far
 // below the sums' tolerance.  CLAMP: the values may hold -inf (weight 0, and no 0 * inf).
-template <int N, bool CLAMP>
-__device__ __forceinline__ void ft_stat_acc(FtStat &st, const float (&f)[N], float vmax)
+// Move the reference of (m, s, t) up to vmax when vmax exceeds it.
+__device__ __forceinline__ void ft_stat_rebase(FtStat &st, float vmax)
 {
-    if (vmax == -INFINITY)
-        return;
     if (vmax > st.m) {
         if (st.m == -INFINITY) {
             st.s = 0.0f;
@@ -124,6 +122,14 @@ __device__ __forceinline__ void ft_stat_acc(FtStat &st, const float (&f)[N], flo
         }
         st.m = vmax;
     }
+}
+
+template <int N, bool CLAMP>
+__device__ __forceinline__ void ft_stat_acc(FtStat &st, const float (&f)[N], float vmax)
+{
+    if (vmax == -INFINITY)
+        return;
+    ft_stat_rebase(st, vmax);
     const float ml = st.m * kFtL2e;
 #pragma unroll
     for (int h = 0; h < N; ++h) {
@@ -304,6 +310,40 @@ __device__ __forceinline__ bool ft_scan_bf16(const FtParams &p, int64_t rowb, in
         for (int q = 0; q < kFtLoads; ++q) {
             const int64_t v = v0 + q * 32 + lane;
             x[q] = v < nv ? __ldg(src + v) : make_uint4(kFtNegInf2, kFtNegInf2, kFtNegInf2, kFtNegInf2);
+        }
+        if (v0 + kFtLoads * 32 <= nv) {
+            // a full batch (warp-uniform): the top-4 updates and the batch maximum, one
+            // rebase, then the statistics of all 64 values in two chains
+            uint32_t b2 = kFtLow2;
+#pragma unroll
+            for (int q = 0; q < kFtLoads; ++q) {
+                const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    ft_top4(T0[k], T1[k], T2[k], T3[k], w[k]);
+                    b2 = bf16x2_max(b2, w[k]);
+                }
+            }
+            ft_stat_rebase(st, ft_hmax(b2));
+            const float ml = st.m * kFtL2e;
+            float s0 = 0.0f, s1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
+#pragma unroll
+            for (int q = 0; q < kFtLoads; ++q) {
+                const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t c = bf16x2_max(w[k], kFtLow2);
+                    const float d0 = fmaf(bf16_lo(c), kFtL2e, -ml), d1 = fmaf(bf16_hi(c), kFtL2e, -ml);
+                    const float e0 = fast_exp2(d0), e1 = fast_exp2(d1);
+                    s0 += e0;
+                    s1 += e1;
+                    t0 = fmaf(e0, d0, t0);
+                    t1 = fmaf(e1, d1, t1);
+                }
+            }
+            st.s += s0 + s1;
+            st.t += t0 + t1;
+            continue;
         }
 #pragma unroll
         for (int q = 0; q < kFtLoads; ++q) {
