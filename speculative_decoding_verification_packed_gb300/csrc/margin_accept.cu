@@ -223,16 +223,29 @@ __device__ __forceinline__ Top2 scan_chunk_warp(const MarginArgs &a, int64_t row
     return t;
 }
 
-__device__ void finish_request(const MarginArgs &a, int32_t i)
+// Greedy acceptance of request i by one warp, once every row argmax is in: lane l compares
+// candidate j0 + l with the argmax of the row before it, and the first mismatch (ballot)
+// ends the accepted prefix.
+__device__ void finish_request(const MarginArgs &a, int32_t i, int lane)
 {
     const int32_t off = __ldcg(a.cu_slots + i);
     const int32_t k = __ldcg(a.cu_slots + i + 1) - off;
-    int32_t acc = 0;
-    while (acc + 1 < k && __ldg(a.tokens + off + acc + 1) == __ldcg(a.row_argmax + off + acc))
-        ++acc;
-    a.accept_len[i] = 1 + acc;
-    a.next_token[i] = __ldcg(a.row_argmax + off + acc);
-    for (int32_t j = 0; j < k; ++j)      // the workspace returns to zero
+    int32_t acc = k - 1;
+    for (int32_t j0 = 1; j0 < k; j0 += 32) {
+        const int32_t j = j0 + lane;
+        const bool miss = j < k && __ldg(a.tokens + off + j) != __ldcg(a.row_argmax + off + j - 1);
+        const uint32_t m = __ballot_sync(0xffffffffu, miss);
+        if (m) {
+            acc = j0 + __ffs(m) - 2;
+            break;
+        }
+    }
+    if (lane == 0) {
+        a.accept_len[i] = 1 + acc;
+        a.next_token[i] = __ldcg(a.row_argmax + off + acc);
+    }
+    __syncwarp();
+    for (int32_t j = lane; j < k; j += 32)   // the workspace returns to zero
         a.row_argmax[off + j] = 0;
 }
 
@@ -289,6 +302,7 @@ __global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
             pp[k] = Top2{0.0f, 0.0f, 0};
         }
         r = top2_warp_merge(r);
+        int32_t fin = -1;   // request whose last row this is
         if (lane == 0) {
             a.row_ticket[row] = 0;
             if (a.top1_idx) a.top1_idx[row] = r.i1;
@@ -303,9 +317,14 @@ __global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
                 if (atomicAdd(a.req_ticket + i, 1) == k - 1) {
                     __threadfence();
                     a.req_ticket[i] = 0;
-                    finish_request(a, i);
+                    fin = i;
                 }
             }
+        }
+        fin = __shfl_sync(0xffffffffu, fin, 0);
+        if (fin >= 0) {
+            __syncwarp();   // lane 0's acquire (ticket + fence) orders the other lanes' reads
+            finish_request(a, fin, lane);
         }
     }
 
