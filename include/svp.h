@@ -294,6 +294,25 @@ svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, int32_t w,
 svp_status svp_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes,
                            const int32_t *idx, int32_t rows, void *dst, void *stream);
 
+/*
+ * The same for up to SVP_GATHER_MAX_FIELDS fields that share one row map, in one launch
+ * (a step packs its query, key, value and logit rows together).  fields: a HOST array of
+ * n_fields descriptors (1 <= n_fields <= SVP_GATHER_MAX_FIELDS), read during the call and
+ * not retained; each src / dst pair follows the rules of svp_gather_rows (16-byte aligned,
+ * row_bytes a multiple of 16, SVP_EUNSUPPORTED otherwise); dst of field f holds
+ * [rows, row_bytes_f].  idx [rows] int32, shared.  No workspace.
+ */
+#define SVP_GATHER_MAX_FIELDS 8
+typedef struct {
+    const void *src;    /* [src_rows, row_bytes] */
+    int64_t src_rows;
+    int64_t row_bytes;
+    void *dst;          /* [rows, row_bytes] */
+} svp_gather_field;
+
+svp_status svp_gather_rows_multi(const svp_gather_field *fields, int32_t n_fields,
+                                 const int32_t *idx, int32_t rows, void *stream);
+
 /* ---------------------------------------------------------------------------------- */
 /* Stochastic prefix verifier, temperature T > 0 (DScale SIII-D, Prefix verifier).       */
 /*   P_r = softmax(logits[r] / T).  Candidate j of request i (tokens[off_i + j],          */

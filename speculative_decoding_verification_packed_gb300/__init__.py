@@ -54,6 +54,13 @@ class svp_kv(ctypes.Structure):
                 ("stride_tok", ctypes.c_int64)]
 
 
+class svp_gather_field(ctypes.Structure):
+    _fields_ = [("src", ctypes.c_void_p), ("src_rows", ctypes.c_int64),
+                ("row_bytes", ctypes.c_int64), ("dst", ctypes.c_void_p)]
+
+
+GATHER_MAX_FIELDS = 8
+
 _lib = None
 
 _SIGS = {
@@ -102,6 +109,9 @@ _SIGS = {
     "svp_gather_rows": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32,
         ctypes.c_void_p, ctypes.c_void_p]),
+    "svp_gather_rows_multi": (ctypes.c_int, [
+        ctypes.POINTER(svp_gather_field), ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+        ctypes.c_void_p]),
     "svp_stochastic_accept_workspace_size": (ctypes.c_int, [
         ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]),
     "svp_stochastic_accept": (ctypes.c_int, [
@@ -448,6 +458,23 @@ def dvl_allocate_pack(scores, *, n_live=None, budget_per_req: int = 8, m_cap: Op
     _check(st, "svp_dvl_allocate_pack")
     out["ws"] = ws
     return out
+
+
+def gather_rows_multi(srcs, idx, *, outs=None, stream=None):
+    """svp_gather_rows_multi: the packed copy of several wide per-row fields sharing the row
+    map idx, in one launch; returns the list of outputs."""
+    rows = idx.shape[0]
+    if not 1 <= len(srcs) <= GATHER_MAX_FIELDS:
+        raise ValueError(f"gather_rows_multi takes 1..{GATHER_MAX_FIELDS} fields")
+    if outs is None:
+        outs = [torch.empty((rows,) + tuple(s.shape[1:]), dtype=s.dtype, device=s.device) for s in srcs]
+    fields = (svp_gather_field * len(srcs))()
+    for f, (s, o) in enumerate(zip(srcs, outs)):
+        rb = s[0].numel() * s.element_size() if s.shape[0] else o[0].numel() * o.element_size()
+        fields[f] = svp_gather_field(_dev(s, f"srcs[{f}]"), s.shape[0], rb, _dev(o, f"outs[{f}]"))
+    _check(lib().svp_gather_rows_multi(fields, len(srcs), _dev(idx, "idx", torch.int32), rows,
+                                       _stream(stream)), "svp_gather_rows_multi")
+    return outs
 
 
 def gather_rows(src, idx, *, out=None, stream=None):

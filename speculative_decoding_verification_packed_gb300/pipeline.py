@@ -6,8 +6,8 @@ shapes from step to step, boundaries change only through device values, and the 
 step (allocate and pack, verify, accept) is captured once per request bucket and replayed
 with no host readback.
 
-This module only orders calls into the library (svp_dvl_allocate_pack, svp_gather_rows,
-svp_verify_attn_packed, svp_margin_accept); every step of the computation runs in the
+This module only orders calls into the library (svp_dvl_allocate_pack,
+svp_gather_rows_multi, svp_verify_attn_packed, svp_margin_accept); every step of the computation runs in the
 library's kernels.  The wide per-slot fields a target model would produce for the packed
 rows (query / key / value rows, target logits) are given here at full block width,
 [n_bs * w, ...], and packed by the row references the packer writes (row i * w + j for
@@ -19,7 +19,7 @@ from typing import Optional
 
 import torch
 
-from . import (dvl_allocate_pack, gather_rows, margin_accept, margin_accept_workspace_size,
+from . import (dvl_allocate_pack, gather_rows_multi, margin_accept, margin_accept_workspace_size,
                verify_attn_packed, verify_attn_workspace_size, Workspace, make_kv)
 
 
@@ -80,11 +80,8 @@ class VerifyPipeline:
                               m_cap=self.m_cap, tokens=self.tokens, positions=self.positions,
                               kv_refs=self.row_ids, fill_token=0, fill_pos=0, fill_ref=-1,
                               ws=self.ws_dvl, stream=stream)
-        refs = a["kv_refs"]
-        gather_rows(self.q_full, refs, out=self.q, stream=stream)
-        gather_rows(self.k_full, refs, out=self.k_new, stream=stream)
-        gather_rows(self.v_full, refs, out=self.v_new, stream=stream)
-        gather_rows(self.logits_full, refs, out=self.logits, stream=stream)
+        gather_rows_multi([self.q_full, self.k_full, self.v_full, self.logits_full], a["kv_refs"],
+                          outs=[self.q, self.k_new, self.v_new, self.logits], stream=stream)
         verify_attn_packed(self.q, self.k_new, self.v_new, self.ctx_len, a["cu_slots"], w=self.w,
                            hkv=self.hkv, kv=self.kv, out=self.out, lse=self.lse, ws=self.ws_attn,
                            stream=stream)

@@ -104,3 +104,34 @@ def test_no_fields_and_bad_live_count():
     # budget beyond m_cap
     g, _, ws = _run(s, 10, 8, 79, fields=False, reference=False)
     assert ws.read_status() == svp.DEV_BAD_SLOTS
+
+
+def test_gather_rows_single_and_multi():
+    """Row-mapped packing of wide fields: dst[r] = src[idx[r]] for ids in range, zeros
+    otherwise (the packer's placeholder reference -1 and ids past the source), for one field
+    and for four fields of different widths in one launch."""
+    g = torch.Generator().manual_seed(3)
+    src_rows, rows = 37, 29
+    idx = torch.randint(-1, src_rows + 3, (rows,), generator=g, dtype=torch.int32)
+    idx[0], idx[1], idx[2] = -1, src_rows, src_rows - 1
+    fields = [torch.randn(src_rows, 8, 16, generator=g).to(torch.bfloat16),
+              torch.randn(src_rows, 2, 16, generator=g).to(torch.bfloat16),
+              torch.randint(0, 1 << 20, (src_rows, 4), generator=g, dtype=torch.int32),
+              torch.randn(src_rows, 1000, generator=g)]
+
+    def expect(src):
+        out = torch.zeros((rows,) + tuple(src.shape[1:]), dtype=src.dtype)
+        for r in range(rows):
+            if 0 <= int(idx[r]) < src_rows:
+                out[r] = src[int(idx[r])]
+        return out
+
+    d_idx = idx.cuda()
+    one = svp.gather_rows(fields[0].cuda(), d_idx)
+    outs = svp.gather_rows_multi([f.cuda() for f in fields], d_idx)
+    torch.cuda.synchronize()
+    assert torch.equal(one.cpu(), expect(fields[0]))
+    for f, o in zip(fields, outs):
+        assert torch.equal(o.cpu(), expect(f))
+    with pytest.raises(ValueError):
+        svp.gather_rows_multi([fields[0].cuda()] * (svp.GATHER_MAX_FIELDS + 1), d_idx)
