@@ -369,6 +369,10 @@ extern "C" svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, i
     p.ref_packed = ref_packed;
     p.n_adjust = n_adjust;
     p.status = static_cast<int32_t *>(ws);
-    dvl_kernel<<<1, kDvlThreads, sizeof(DvlShared), (cudaStream_t)stream>>>(p);
+    // small batches (at most one candidate slot per thread of a quarter block) run a quarter
+    // block: every loop of the kernel strides by the block size, and fewer warps meet at
+    // each of its barriers
+    const int threads = (int64_t)n_bs * w <= kDvlThreads / 4 ? kDvlThreads / 4 : kDvlThreads;
+    dvl_kernel<<<1, threads, sizeof(DvlShared), (cudaStream_t)stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
 }
