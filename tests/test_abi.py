@@ -72,6 +72,26 @@ def test_invalid_arguments_rejected_on_host(L):
     # empty batch is a no-op
     assert L.svp_verify_attn_packed(None, None, None, ctypes.byref(kv), None, None, 0, 0, 16,
                                     ctypes.byref(h), 1, None, None, 1, 1 << 20, None) == svp.SVP_OK
+    # multi-field gather: field count, row width and alignment are checked on the host
+    fields = (svp.svp_gather_field * 9)()
+    for f in range(9):
+        fields[f] = svp.svp_gather_field(1 << 12, 4, 64, 1 << 16)
+    assert L.svp_gather_rows_multi(fields, 0, 1 << 20, 4, None) == svp.SVP_EINVAL
+    assert L.svp_gather_rows_multi(fields, 9, 1 << 20, 4, None) == svp.SVP_EINVAL
+    assert L.svp_gather_rows_multi(fields, 2, None, 4, None) == svp.SVP_EINVAL
+    fields[1] = svp.svp_gather_field(1 << 12, 4, 8, 1 << 16)       # row narrower than 16 bytes
+    assert L.svp_gather_rows_multi(fields, 2, 1 << 20, 4, None) == svp.SVP_EINVAL
+    fields[1] = svp.svp_gather_field(1 << 12, 4, 24, 1 << 16)      # not a multiple of 16
+    assert L.svp_gather_rows_multi(fields, 2, 1 << 20, 4, None) == svp.SVP_EUNSUPPORTED
+    fields[1] = svp.svp_gather_field(1 << 12, 4, 64, 1 << 16)
+    assert L.svp_gather_rows_multi(fields, 8, 1 << 20, 0, None) == svp.SVP_OK   # no rows
+
+
+def test_gather_binding_field_count():
+    import torch
+    x = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        svp.gather_rows_multi([x] * (svp.GATHER_MAX_FIELDS + 1), torch.zeros(4, dtype=torch.int32))
 
 
 def test_binding_refuses_cpu_tensors():
