@@ -747,13 +747,9 @@ template <int D>
 static svp_status launch_d(const TcParams &p, int grid, cudaStream_t stream)
 {
     using C = TcCfg<D>;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM) != cudaSuccess)
-            return SVP_ECUDA;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    if (set_smem_limit_once(attn_tc_kernel<D>, C::SMEM, configured) != cudaSuccess)
+        return SVP_ECUDA;
     attn_tc_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
 }

@@ -341,13 +341,9 @@ extern "C" svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, i
         return SVP_EUNSUPPORTED;
     if (ws_bytes < kWsHeader)
         return SVP_EWORKSPACE;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(dvl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sizeof(DvlShared)) != cudaSuccess)
-            return SVP_ECUDA;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    if (set_smem_limit_once(dvl_kernel, (int)sizeof(DvlShared), configured) != cudaSuccess)
+        return SVP_ECUDA;
     DvlParams p;
     p.scores = scores;
     p.n_live = n_live;

@@ -3,6 +3,7 @@
 // Inline PTX written from the public PTX ISA; no library code.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -393,6 +394,25 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 __device__ __forceinline__ void named_bar_arrive(int id, int nthreads)
 {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Host: raise a kernel's dynamic shared-memory limit once per (kernel, device).  `done`
+// is the call site's bit set over device ordinals; a concurrent first call on the same
+// device just sets the attribute twice.
+template <typename K>
+inline cudaError_t set_smem_limit_once(K kernel, int bytes, std::atomic<uint64_t> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit)
+        done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 __device__ __forceinline__ void set_status(int32_t *status, int32_t bits)
