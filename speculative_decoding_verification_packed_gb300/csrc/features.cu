@@ -10,7 +10,9 @@
 // units fill the GPU's resident warps once; the chunks of a row are merged by the last warp
 // to take the row's ticket.
 //  * Softmax statistics per lane: an online (max m, s = sum 2^d, t = sum 2^d d) with
-//    d = (z - m) log2 e; entropy = ln s - t ln2 / s, log-sum-exp = m + ln s.
+//    d = (z - m) log2 e; entropy = ln s - t ln2 / s, log-sum-exp = m + ln s.  bf16 rows
+//    rebase (m, s, t) once per full batch of eight 16-byte vectors (batch maximum by packed
+//    max).
 //  * Top-16, bf16 rows: each lane's 8 streams (packed word k of its 16-byte vectors, low or
 //    high half) keep their top 4 with packed bf16 min / max, branch-free; 16 rounds of warp
 //    maximum draw the chunk's top-16 from those entries.  Exact unless a stream's fourth

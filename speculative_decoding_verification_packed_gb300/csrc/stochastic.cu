@@ -12,9 +12,11 @@
 // eight 16-byte loads in flight per lane, the chunk sized so that the units of m_cap rows
 // fill the GPU's resident warps once: the chunk's (max, sum of
 // 2^((z - max) log2(e) / T)) is kept per chunk and merged per row by the last warp to take
-// the row's ticket.  HBM-bound over the live logit rows.  (2) One block per request: warp 0
-// tests every candidate at once (probabilities from the row statistics, first rejection by
-// ballot), then walks the chunk masses of the successor row in token order to the chunk
+// the row's ticket; bf16 batches take their maximum by packed max and rebase the sum once.
+// HBM-bound over the live logit rows.  (2) One block per request: warp 0 tests every
+// candidate at once (probabilities from the row statistics, first rejection by ballot)
+// while the other warps bring the chunk statistics of the request's rows into shared
+// memory, then walks the chunk masses of the successor row in token order to the chunk
 // that holds the draw; the block rescans only that chunk (block prefix sum of per-thread
 // masses, then one thread's elements in order).
 #include <cstdint>
