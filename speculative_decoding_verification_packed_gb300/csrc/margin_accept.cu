@@ -21,7 +21,8 @@
 //     lowest index), so results do not depend on arrival order.
 //   * The warp that finishes the last chunk of a row (atomic ticket, no waiting)
 //     finalises the row; in the fused kernel the warp that finalises the last row of a
-//     request then runs the greedy acceptance for that request.  Tickets, partials and
+//     request then runs the greedy acceptance for that request, all candidates at once
+//     (lane l compares candidate l, the first mismatch by ballot).  Tickets, partials and
 //     per-row argmaxes are cleared by their last reader, so the workspace is all zero
 //     again after every call and can serve calls of any size.
 #include <cfloat>
