@@ -256,7 +256,17 @@ def capture_step(plan, stream):
     return graphs
 
 
-def timed_run(sets, steps, warmup, svp, tile_mode=None, clocks=None):
+def launch_dist(times_ms):
+    """Median and nearest-rank p10 / p90 of per-launch device times (ms in, us out)."""
+    xs = sorted(times_ms)
+    if not xs:
+        return None
+    rank = lambda q: xs[min(len(xs) - 1, max(0, int(round(q * (len(xs) - 1)))))]
+    return {"median": round(statistics.median(xs) * 1e3, 2), "p10": round(rank(0.1) * 1e3, 2),
+            "p90": round(rank(0.9) * 1e3, 2)}
+
+
+def timed_run(sets, steps, warmup, svp, tile_mode=None, clocks=None, dist_out=None):
     """K steps rotating over the input sets, each step replayed from captured graphs
     (no host work inside the timed region); per-launch device times from events
     recorded on the stream around each launch."""
@@ -292,6 +302,9 @@ def timed_run(sets, steps, warmup, svp, tile_mode=None, clocks=None):
     per_launch = [statistics.mean(ev[s][li][0].elapsed_time(ev[s][li][1]) for s in range(steps))
                   for li in range(nl)]
     names = [n for n, _ in graphs[0]]
+    if dist_out is not None:
+        for li, name in enumerate(names):
+            dist_out[name] = launch_dist([ev[s][li][0].elapsed_time(ev[s][li][1]) for s in range(steps)])
     return total_ms, dict(zip(names, per_launch)), clk, wall, steps * nl
 
 
@@ -412,8 +425,9 @@ def run_ours(args):
     sets = probe + make_sets(args.workload, nsets - 1, args.seed + 1000 * rank + 1, dev)
     clocks = ClockSampler(local)
     barrier(world)
+    dist = {}
     total_ms, per_launch, clk, wall, launches = timed_run(sets, args.steps, args.warmup, svp,
-                                                          clocks=clocks)
+                                                          clocks=clocks, dist_out=dist)
     total_ms = reduce_max(total_ms, world)
     rows = reduce_sum(sum(int(sets[s % nsets].cu_slots[-1]) for s in range(args.steps)), world)
     ms_step = total_ms / args.steps
@@ -440,6 +454,7 @@ def run_ours(args):
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
         "kv_gbs": round(achieved, 1),
         "per_launch_us": {k: round(v * 1e3, 2) for k, v in per_launch.items()},
+        "per_launch_us_dist": dist,
         "gpu_launches": launches,
         "clocks": clk,
     }

@@ -54,3 +54,12 @@ def test_single_rank_is_identity():
     import bench
     assert bench.reduce_max(3.5, 1) == 3.5
     assert bench.reduce_sum(7.0, 1) == 7.0
+
+
+def test_launch_distribution_summary():
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.launch_dist([0.05, 0.01, 0.02, 0.03, 0.04, 0.06, 0.07, 0.08, 0.09, 0.10, 0.11])
+    assert d == {"median": 60.0, "p10": 20.0, "p90": 100.0}
+    assert bench.launch_dist([0.042]) == {"median": 42.0, "p10": 42.0, "p90": 42.0}
+    assert bench.launch_dist([]) is None
