@@ -32,7 +32,9 @@
  *     it grows with n); the attention workspace is tied to one head_dim and tile mode
  *     (a mismatch is reported as SVP_DEV_WORKSPACE and nothing is computed).  Kernels
  *     leave their counters at zero when they finish.  Calls that share one workspace
- *     must not overlap on the GPU.  After SVP_DEV_TIMEOUT, zero the workspace again.
+ *     must not overlap on the GPU.  After SVP_DEV_TIMEOUT, zero the workspace again:
+ *     until then an attention call on it computes nothing and reports SVP_DEV_WORKSPACE
+ *     (its split-KV tickets may have been left mid-count).
  *   - Rows of out/lse that belong to no request (rows >= cu_slots[n], padding) are
  *     never written.
  *   - Kernels never trap.  Every wait inside a kernel is bounded; on expiry the kernel
@@ -231,8 +233,9 @@ svp_status svp_margin_accept(const void *logits, int64_t row_stride, int32_t m_c
 /* the library until the process exits; sizes whose workspace                           */
 /* (svp_margin_accept_workspace_size) exceeds 2 MiB return SVP_EWORKSPACE and nothing   */
 /* is enqueued.  The first call on each device (with that device current) looks up the  */
-/* array's device address and clears it once (cudaGetSymbolAddress, cudaMemset; no      */
-/* allocation), so make that first call before capturing any stream.  All calls share   */
+/* array's device address and clears it once on `stream`, waiting for that stream       */
+/* (cudaGetSymbolAddress, cudaMemsetAsync, cudaStreamSynchronize; no allocation), so    */
+/* make that first call before capturing any stream.  All calls share                   */
 /* the one array: calls that overlap on the GPU (other streams, other host threads)     */
 /* race and must be serialised by the caller.  The kernel leaves the array zeroed.      */
 /* Device-side metadata errors are not reported through a status word in this variant:  */

@@ -267,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (tid == 0) {
         // the workspace layout must match this call's (head_dim, tile mode)
         const int32_t seen = *reinterpret_cast<volatile int32_t *>(p.status + 1);
-        *flag_last = (seen != 0 && seen != p.sig) ? 1 : 0;
+        const int32_t poisoned = *reinterpret_cast<volatile int32_t *>(p.status + kWsPoisonWord);
+        *flag_last = ((seen != 0 && seen != p.sig) || poisoned != 0) ? 1 : 0;
         if (*flag_last && blockIdx.x == 0)
             set_status(p.status, SVP_DEV_WORKSPACE);
         if (seen == 0 && blockIdx.x == 0)
@@ -380,11 +381,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 }
                 u += (s.t1 - s.t0);
             }
+            const uint32_t first = it > (uint32_t)C::STAGES ? it - C::STAGES : 0;
             if (!ok) {
                 // drain: wait (bounded) for every stage armed but not yet consumed
                 volatile int drain_abort = 0;
-                for (uint32_t k = (it > (uint32_t)C::STAGES ? it - C::STAGES : 0); k < it; ++k)
+                for (uint32_t k = first; k < it; ++k)
                     mbar_wait(bar_full(k % C::STAGES), (k / C::STAGES) & 1, &drain_abort);
+            } else {
+                // tail: the release of every stage (a tensor-core commit on bar_empty) has
+                // landed before the CTA exits
+                for (uint32_t k = first; k < it; ++k)
+                    mbar_wait(bar_empty(k % C::STAGES), (k / C::STAGES) & 1, abort_flag);
             }
         }
     } else if (warp == 1) {
@@ -461,6 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             tc_commit(bar_drain);
             volatile int drain_abort = 0;
             mbar_wait(bar_drain, 0, &drain_abort);
+            // tail: the arrives of the last Q-release and S-buffer commits have landed
+            if (ok && nseg > 0)
+                mbar_wait(bar_qempty, (nseg - 1) & 1, abort_flag);
+            for (uint32_t back = 1; ok && back <= 2 && back <= it; ++back)
+                mbar_wait(bar_sfull((it - back) & 1), ((it - back) >> 1) & 1, abort_flag);
         }
     } else {
         // ============================================================ softmax / epilogue
@@ -470,7 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int stid = tid - kSoftmaxWarp0 * 32;        // 0..127
         uint32_t it = 0, nseg = 0;
         bool ok = true;
-        for (int64_t u = cta_s; u < cta_e && ok;) {
+        // A wait that gives up does not leave the loops: the thread runs on (later waits
+        // return at once) and the four warps leave together at the next barrier they share.
+        for (int64_t u = cta_s; u < cta_e;) {
             Seg s;
             make_seg(p, sh, u, cta_e, cta_s, s);
             const int32_t off = __ldg(p.cu_slots + s.i);
@@ -501,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     kvalid = min(kBN, L - t * kBN);
                 else
                     kvalid = max(0, min(CB, min(k_i, (s.rb + 1) * p.R) - (t - s.n_ctx) * CB));
-                if (!(ok = mbar_wait(bar_sfull(b), (it >> 1) & 1, abort_flag)))
-                    break;
+                ok &= mbar_wait(bar_sfull(b), (it >> 1) & 1, abort_flag);
+                __syncwarp();
                 tc_fence_after();
                 float sv[kBN];
                 if (warp_active) {
@@ -548,8 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     m_run = m_new;
                 }
                 // P (shared) and O (TMEM) are in use by PV of the previous tile
-                if (it > 0 && !(ok = mbar_wait(bar_pvdone, (it - 1) & 1, abort_flag)))
-                    break;
+                if (it > 0)
+                    ok &= mbar_wait(bar_pvdone, (it - 1) & 1, abort_flag);
+                __syncwarp();
                 tc_fence_after();
                 if (k > 0 && __any_sync(0xffffffffu, grow && active)) {
                     // rescale this warp's rows of O
@@ -600,11 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 if (lane == 0)
                     mbar_arrive(bar_pfull);
             }
-            if (!ok)
-                break;
             // ---- epilogue: O of this segment is complete after the last PV
-            if (!(ok = mbar_wait(bar_pvdone, (it - 1) & 1, abort_flag)))
-                break;
+            ok &= mbar_wait(bar_pvdone, (it - 1) & 1, abort_flag);
+            __syncwarp();
             tc_fence_after();
             const int32_t h = s.hg * p.HP + hh;
             const int64_t orow = (int64_t)(off + j) * p.hq + h;
@@ -660,7 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 if (lane == 0)
                     mbar_arrive(bar_ofree);
                 __threadfence();
-                named_bar_sync(1, 128);
+                if (named_bar_any(1, 128, !ok))
+                    break;   // all four warps leave here together
                 if (stid == 0) {
                     const int32_t C0 = ncta;
                     const int32_t cf = cta_of_unit(s.u_pair0, sh.total, C0);
@@ -733,8 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
 
     // ---------------------------------------------------------------- teardown
-    if (*abort_flag && tid == 0)
+    if (*abort_flag && tid == 0) {
         set_status(p.status, SVP_DEV_TIMEOUT);
+        *reinterpret_cast<volatile int32_t *>(p.status + kWsPoisonWord) = 1;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

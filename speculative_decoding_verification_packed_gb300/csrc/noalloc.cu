@@ -12,9 +12,11 @@
 // that loads the library holds it until the process exits.  Host code cannot use the
 // array's name as a device address, so on the first call on each device (with that
 // device current) the library asks the runtime for the array's device address with
-// cudaGetSymbolAddress, checks the result, and clears the array once (cudaMemset, which
-// does not allocate).  After that the kernel leaves the scratch all zero at the end of
-// every call, as the fused kernel always does with its workspace.
+// cudaGetSymbolAddress, checks the result, and clears the array once: a cudaMemsetAsync on
+// the caller's stream, then a wait for that stream, so the clear is complete before any
+// kernel on any stream uses the array (neither call allocates).  After that the kernel
+// leaves the scratch all zero at the end of every call, as the fused kernel always does
+// with its workspace.
 #include <mutex>
 
 #include "svp_device.cuh"
@@ -39,8 +41,10 @@ std::mutex g_setup_mutex;
 void *g_scratch_addr[kMaxDevices] = {nullptr};
 }  // namespace
 
-// Device address of this device's scratch, set up on first use (nullptr on failure).
-static void *noalloc_scratch_for_current_device(svp_status *err)
+// Device address of this device's scratch, set up on first use (nullptr on failure).  The
+// first use clears the array on `stream` and waits for it before the address is handed
+// out, so a first call made on a non-blocking stream cannot race the clear.
+static void *noalloc_scratch_for_current_device(cudaStream_t stream, svp_status *err)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -54,7 +58,8 @@ static void *noalloc_scratch_for_current_device(svp_status *err)
             *err = SVP_ECUDA;
             return nullptr;
         }
-        if (cudaMemset(ptr, 0, kNoAllocScratchBytes) != cudaSuccess) {
+        if (cudaMemsetAsync(ptr, 0, kNoAllocScratchBytes, stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess) {
             *err = SVP_ECUDA;
             return nullptr;
         }
@@ -83,7 +88,7 @@ extern "C" svp_status svp_margin_accept_noalloc(const void *logits, int64_t row_
     if (need > kNoAllocScratchBytes)
         return SVP_EWORKSPACE;   // sizes beyond the fixed scratch: use svp_margin_accept
     svp_status err = SVP_OK;
-    void *scratch = noalloc_scratch_for_current_device(&err);
+    void *scratch = noalloc_scratch_for_current_device((cudaStream_t)stream, &err);
     if (!scratch)
         return err;
     return margin_launch(logits, row_stride, m_cap, vocab, dtype, top1_idx, top1, top2, margin,

@@ -13,8 +13,12 @@
 
 namespace svp {
 
-// Workspace header shared by every entry point: [0] device status word.
+// Workspace header shared by every entry point: [0] device status word, [1] layout
+// signature (attention), [2] poison word: set by a launch that gave up on a bounded wait
+// (its pair tickets and partials may be left mid-flight), cleared only by
+// svp_workspace_init; an attention launch that finds it set computes nothing.
 constexpr size_t kWsHeader = 256;
+constexpr int kWsPoisonWord = 2;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -106,6 +110,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 {
     if (mbar_try_wait(bar, parity))
         return true;
+    if (*abort_flag)
+        return false;   // another role has given up already
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (SVP_WAIT_SLEEP_NS > 0 ? mbar_try_wait_sleep(bar, parity, SVP_WAIT_SLEEP_NS)
@@ -114,7 +120,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
         if ((it & 15u) == 0) {
             if (*abort_flag)
                 return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            // signed difference: a timer that steps back never reads as an expiry
+            if ((int64_t)(global_ns() - t0) > (int64_t)kWaitLimitNs) {
                 *abort_flag = 1;
                 return false;
             }
@@ -394,6 +401,24 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 __device__ __forceinline__ void named_bar_arrive(int id, int nthreads)
 {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a flag over its participants: every thread gets true when
+// any of them passed true.  Roles that give up on a bounded wait keep running to the next
+// such barrier and all of them leave together, so no thread is left waiting at a barrier
+// that the others will never reach.
+__device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool flag)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)flag), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // Host: raise a kernel's dynamic shared-memory limit once per (kernel, device).  `done`

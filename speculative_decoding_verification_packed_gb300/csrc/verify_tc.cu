@@ -414,6 +414,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
     int32_t *ctile = cprefix + (NQ + 1);                                  // [gridDim.x + 1]
     // start the workspace-signature load early; it is checked after the prologue
     const int32_t sig_seen = (tid == 0) ? *reinterpret_cast<volatile int32_t *>(p.status + 1) : 0;
+    const int32_t poison_seen =
+        (tid == 0) ? *reinterpret_cast<volatile int32_t *>(p.status + kWsPoisonWord) : 0;
 
     if (tid == 0) {
         for (int s = 0; s < nslot; ++s) {
@@ -516,9 +518,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
     if (bad_bits && blockIdx.x == 0)
         set_status(p.status, bad_bits);
     if (tid == 0) {
-        // the workspace layout must match this call's (head_dim, tile mode)
+        // the workspace layout must match this call's (head_dim, tile mode), and no earlier
+        // launch may have given up mid-flight (its tickets would be stale)
         const int32_t seen = sig_seen;
-        rs->last = (seen != 0 && seen != p.sig) ? 1 : 0;
+        rs->last = ((seen != 0 && seen != p.sig) || poison_seen != 0) ? 1 : 0;
         if (rs->last && blockIdx.x == 0)
             set_status(p.status, SVP_DEV_WORKSPACE);
         if (seen == 0 && blockIdx.x == 0)
@@ -622,11 +625,20 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             }
             u += (s.t1 - s.t0);
         }
-        if (!ok && lane == 0) {
-            volatile int drain_abort = 0;
+        if (lane == 0) {
             const uint32_t first = seq > (uint32_t)nslot ? seq - nslot : 0;
-            for (uint32_t k = first; k < seq; ++k)
-                mbar_wait(bar_full(k % nslot), (k / nslot) & 1, &drain_abort);
+            if (!ok) {
+                // the loads already issued land before the CTA exits
+                volatile int drain_abort = 0;
+                for (uint32_t k = first; k < seq; ++k)
+                    mbar_wait(bar_full(k % nslot), (k / nslot) & 1, &drain_abort);
+            } else {
+                // tail: the release of every fill (a tensor-core commit arriving on
+                // bar_empty) has landed before the CTA exits, so no asynchronous arrive
+                // reaches this shared memory after it is handed to another CTA
+                for (uint32_t k = first; k < seq; ++k)
+                    mbar_wait(bar_empty(k % nslot), (k / nslot) & 1, abort_flag);
+            }
         }
     } else if (warp == 1) {
         // ================================================================ S^T issuer
@@ -700,6 +712,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             tc_commit(bar_drain);
             volatile int drain_abort = 0;
             mbar_wait(bar_drain, 0, &drain_abort);
+            // tail: the arrives of this thread's last commits (Q released, last two S
+            // buffers full) have landed before the CTA exits
+            if (ok && nseg > 0)
+                mbar_wait(bar_qempty, (nseg - 1) & 1, abort_flag);
+            for (uint32_t back = 1; ok && back <= 2 && back <= it; ++back)
+                mbar_wait(bar_sfull((it - back) & 1), ((it - back) >> 1) & 1, abort_flag);
         }
     } else if (warp == 6) {
         // ================================================================ PV issuer
@@ -814,6 +832,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
             tc_commit(bar_drain);
             volatile int drain_abort = 0;
             mbar_wait(bar_drain, 0, &drain_abort);
+            // tail: the last pvdone commit of each P buffer has landed
+            for (uint32_t back = 1; ok && back <= (uint32_t)nP && back <= it; ++back)
+                mbar_wait(bar_pvdone(pbuf(it - back)), ppar(it - back), abort_flag);
         }
     } else {
         // ================================================================ softmax
@@ -850,8 +871,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 const int32_t kvalid = vt_kvalid(p, s, tt, L, k_i);
                 const int32_t cbase = is_ctx ? 0 : (tt - s.n_ctx) * p.CB;   // candidate index of key 0
                 const bool key_ok = t < kvalid;
-                if (!(ok = mbar_wait(bar_sfull(b), (it >> 1) & 1, abort_flag)))
-                    break;
+                // A wait that gives up does not leave the loop here: the thread runs on to
+                // the next barrier of the four warps, where all of them leave together.
+                ok &= mbar_wait(bar_sfull(b), (it >> 1) & 1, abort_flag);
+                __syncwarp();
                 tc_fence_after();
                 const uint32_t sa = tmem + lane_off + TM_S + b * NR;
                 const uint32_t pline = sbase + p.off_p + pbuf(it) * PBYTES + t * 128;
@@ -877,7 +900,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                                 rs->m_ref[r] = mine * cl2;
                         }
                     }
-                    named_bar_sync(1, 128);
+                    if (named_bar_any(1, 128, !ok)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 // P of all chunks into registers while PV of the previous tile runs
                 uint32_t pk[4][16];
@@ -899,9 +925,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 }
                 const bool hit = ymax > kSlack;
                 // this P buffer is read by PV of tile it - nP
-                if (it >= (uint32_t)nP &&
-                    !(ok = mbar_wait(bar_pvdone(pbuf(it)), ppar(it - nP), abort_flag)))
-                    break;
+                if (it >= (uint32_t)nP)
+                    ok &= mbar_wait(bar_pvdone(pbuf(it)), ppar(it - nP), abort_flag);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if (c < nch) {
@@ -914,7 +939,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 }
                 if (__any_sync(0xffffffffu, hit) && lane == 0)
                     rs->flag[it & 1] = 1;
-                named_bar_sync(1, 128);
+                if (named_bar_any(1, 128, !ok)) {
+                    ok = false;
+                    break;
+                }
                 const bool need = rs->flag[it & 1] != 0;
                 if (stid == 0)
                     rs->flag[(it + 1) & 1] = 0;
@@ -933,7 +961,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                         }
                         rs->red[quarter][c * 32 + lane] = warp_transpose_max32(v, lane);
                     }
-                    named_bar_sync(1, 128);
+                    if (named_bar_any(1, 128, !ok)) {
+                        ok = false;
+                        break;
+                    }
                     if (stid < NRs) {
                         const int r = stid;
                         const float mo = rs->m_ref[r];
@@ -951,12 +982,15 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                         }
                         rs->alpha[r] = a;
                     }
-                    named_bar_sync(1, 128);
+                    if (named_bar_any(1, 128, !ok)) {
+                        ok = false;
+                        break;
+                    }
                     if (rs->rescale) {
                         // O^T halves and l^T: column r scaled by alpha[r], once PV of the
                         // previous tile is complete
-                        if (!(ok = mbar_wait(bar_pvdone(pbuf(it - 1)), ppar(it - 1), abort_flag)))
-                            break;
+                        ok &= mbar_wait(bar_pvdone(pbuf(it - 1)), ppar(it - 1), abort_flag);
+                        __syncwarp();
                         tc_fence_after();
                         for (int m = 0; m <= DH; ++m) {
                             const uint32_t base = tmem + lane_off + (m < DH ? TM_O + m * NR : TM_L);
@@ -987,7 +1021,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                             st_shared_v4(pline + blk * 16384 + (((c0 + v) ^ (t & 7)) << 4),
                                          pq[4 * v], pq[4 * v + 1], pq[4 * v + 2], pq[4 * v + 3]);
                     }
-                    named_bar_sync(1, 128);
+                    if (named_bar_any(1, 128, !ok)) {
+                        ok = false;
+                        break;
+                    }
                     if (stid == 0)
                         rs->rescale = 0;
                 }
@@ -1016,14 +1053,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(bar_pfull(pbuf(it)));
-                if (!ok)
-                    break;
             }
             if (!ok)
-                break;
+                break;   // only ever reached by all four warps together (a barrier decided it)
             // ---- epilogue: O^T, l^T complete after the last PV of the segment
-            if (!(ok = mbar_wait(bar_pvdone(pbuf(it - 1)), ppar(it - 1), abort_flag)))
-                break;
+            ok &= mbar_wait(bar_pvdone(pbuf(it - 1)), ppar(it - 1), abort_flag);
+            __syncwarp();
             tc_fence_after();
             // row sums: every lane of l^T holds l for each column
             for (int c = 0; c < nch; ++c) {
@@ -1042,7 +1077,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 const int r = stid;
                 rs->orow[r] = ((int64_t)(out_row0 + r / p.HP) * p.hq + s.hg * p.HP + r % p.HP) * D;
             }
-            named_bar_sync(1, 128);
+            if (named_bar_any(1, 128, !ok)) {
+                ok = false;
+                break;
+            }
             if (stid < nact)
                 rs->linv[stid] = 1.0f / rs->lrow[stid];
             named_bar_sync(1, 128);
@@ -1103,7 +1141,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         // pieces in order.
         if (ok)
             ok = mbar_wait(bar_tick, 0, abort_flag);
+        if (named_bar_any(1, 128, !ok))
+            ok = false;
         const int npend = ok ? rs->npend : 0;
+        if (npend)
+            __threadfence();   // acquire: the other pieces' partials, read below by this thread
         uint32_t merge_phase = 0;
         for (int pi = 0; pi < npend && ok; ++pi) {
             const int32_t *e = rs->pend[pi];
@@ -1170,11 +1212,14 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     p.lse[rs->orow[r] / D] = (M + __log2f(Ls)) * 0.69314718055994531f;
             }
             const int32_t slot0 = rs->pslot[0];
-            for (int32_t c0 = 0; c0 < np && ok; c0 += cap) {
+            for (int32_t c0 = 0; c0 < np; c0 += cap) {
                 const int32_t nb = min(cap, np - c0);
                 const int32_t wq0 = one_block ? c0 : 0;   // weights of this pass: wts[wq0 + q]
                 if (c0 > 0) {
-                    named_bar_sync(1, 128);              // the ring was read by the last pass
+                    if (named_bar_any(1, 128, !ok)) {    // the ring was read by the last pass
+                        ok = false;
+                        break;
+                    }
                     if (stid == 0)
                         issue_pass(c0);
                 }
@@ -1185,8 +1230,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                                                   rs->m_ref[r]);
                 }
                 named_bar_sync(1, 128);
-                if (!(ok = mbar_wait(bar_merge, merge_phase & 1, abort_flag)))
-                    break;
+                const bool landed = mbar_wait(bar_merge, merge_phase & 1, abort_flag);
+                if (!landed && stid == 0) {
+                    volatile int drain_abort = 0;   // the slabs land before the CTA exits
+                    mbar_wait(bar_merge, merge_phase & 1, &drain_abort);
+                }
+                ok &= landed;
                 ++merge_phase;
                 const bool last_pass = c0 + cap >= np;
                 const uint32_t ring = sbase + p.off_ring;
@@ -1210,14 +1259,19 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 if (!last_pass)
                     __threadfence_block();
             }
-            named_bar_sync(1, 128);
+            if (named_bar_any(1, 128, !ok)) {
+                ok = false;
+                break;
+            }
             if (stid == 0)
                 p.tickets[pair] = 0;
         }
     }
 
-    if (*abort_flag && tid == 0)
+    if (*abort_flag && tid == 0) {
         set_status(p.status, SVP_DEV_TIMEOUT);
+        *reinterpret_cast<volatile int32_t *>(p.status + kWsPoisonWord) = 1;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1228,13 +1282,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
 template <int D>
 static svp_status vt_launch_d(const TcParams &p, int grid, cudaStream_t stream)
 {
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(verify_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024) != cudaSuccess)
-            return SVP_ECUDA;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    if (set_smem_limit_once(verify_tc_kernel<D>, 227 * 1024, configured) != cudaSuccess)
+        return SVP_ECUDA;
     verify_tc_kernel<D><<<grid, kVThreads, p.smem_bytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
 }
