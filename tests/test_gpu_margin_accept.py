@@ -98,6 +98,43 @@ def test_margin_accept_wide_vocab_workload():
     _check_rows(b.draft_logits, d)
 
 
+def test_full_vocab_planted_ties_across_chunks():
+    # The launch the bench times (224 rows x 248,320 bf16): each row is cut into chunks
+    # scanned by different warps and CTAs, and the row's maximum is planted twice or three
+    # times in different chunks (or both ends of the row), so the lowest-index rule must
+    # survive the cross-warp, cross-CTA merge of the chunk partials.
+    V, rows = 248320, 224
+    g = torch.Generator().manual_seed(17)
+    x = (torch.randn(rows, V, generator=g) * 2).clamp(-12.0, 12.0).to(torch.bfloat16)
+    pos = torch.randint(0, V, (rows, 3), generator=g)
+    planted = []
+    for r in range(rows):
+        ks = 2 if r % 3 else 3
+        ids = sorted(set(int(v) for v in pos[r, :ks]))
+        if r % 7 == 0:
+            ids = [0, V - 1]                                  # both ends of the row
+        x[r, ids] = 16.0
+        planted.append(min(ids))
+    outs = svp.draft_margin(x.cuda())
+    torch.cuda.synchronize()
+    r_idx = _check_rows(x, outs)
+    assert r_idx.tolist() == planted
+    assert (outs[3].cpu() == 0).all()                         # tied maximum: margin 0
+    # the fused kernel on the same rows: 32 requests of 7 slots, tokens = planted argmaxes
+    cu = torch.arange(0, rows + 1, 7, dtype=torch.int32)
+    tokens = torch.full((rows,), -1, dtype=torch.int32)
+    for i in range(32):
+        for j in range(1, 7):
+            tokens[7 * i + j] = planted[7 * i + j - 1] if j <= (i % 7) else (planted[7 * i + j - 1] + 1) % V
+    fo = svp.margin_accept(x.cuda(), tokens.cuda(), cu.cuda())
+    torch.cuda.synchronize()
+    _check_rows(x, fo)
+    acc, nxt = oracle.greedy_accept(r_idx, tokens, cu)
+    assert np.array_equal(fo[4].cpu().numpy(), acc)
+    assert np.array_equal(fo[5].cpu().numpy(), nxt)
+    assert fo[4].cpu().tolist() == [1 + min(i % 7, 6) for i in range(32)]
+
+
 def test_margin_accept_inactive_and_tail_not_read():
     V = 1000
     g = torch.Generator().manual_seed(3)
