@@ -65,6 +65,8 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the contrast / other-workload measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time only the wide-tile prefill contrast and print its JSON line")
     return ap.parse_args()
 
 
@@ -513,27 +515,7 @@ def run_ours(args):
             extras[other] = e
             del osets
             torch.cuda.empty_cache()
-        # wide-tile prefill contrast: tensor-bound
-        from speculative_decoding_verification_packed_gb300 import workloads as wl
-        q, k, v = wl.make_prefill(device=dev)
-        cu = torch.tensor([0, 4096], dtype=torch.int32, device=dev)
-        pout = torch.empty_like(q)
-        plse = torch.empty((4096, 32), dtype=torch.float32, device=dev)
-        for _ in range(3):
-            svp.prefill_attn(q, k, v, cu, max_s=4096, out=pout, lse=plse)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(10):
-            svp.prefill_attn(q, k, v, cu, max_s=4096, out=pout, lse=plse)
-        e1.record()
-        torch.cuda.synchronize()
-        pms = e0.elapsed_time(e1) / 10
-        flops = 4.0 * 32 * 128 * (4096 * 4097 / 2)
-        extras["prefill_4096_causal"] = {"us": round(pms * 1e3, 1),
-                                         "tflops": round(flops / (pms / 1e3) / 1e12, 1),
-                                         "frac_of_bf16_peak": round(flops / (pms / 1e3) / 1e12 / tf_peak, 4)}
+        extras["prefill_4096_causal"] = prefill_contrast(svp, dev, tf_peak)
         extras.update(next_rows_extras(svp, dev))
         # logit-stream kernels against the same measured HBM copy peak
         for key in ("stochastic_accept", "draft_features"):
@@ -550,6 +532,31 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def prefill_contrast(svp, dev, tf_peak, reps: int = 10):
+    """The wide-tile prefill contrast (tensor-bound): one causal sequence of 4096 rows,
+    32 q / 8 KV heads, d = 128; 3 untimed launches, then `reps` launches timed with events."""
+    import torch
+    from speculative_decoding_verification_packed_gb300 import workloads as wl
+    q, k, v = wl.make_prefill(device=dev)
+    cu = torch.tensor([0, 4096], dtype=torch.int32, device=dev)
+    pout = torch.empty_like(q)
+    plse = torch.empty((4096, 32), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        svp.prefill_attn(q, k, v, cu, max_s=4096, out=pout, lse=plse)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        svp.prefill_attn(q, k, v, cu, max_s=4096, out=pout, lse=plse)
+    e1.record()
+    torch.cuda.synchronize()
+    pms = e0.elapsed_time(e1) / reps
+    flops = 4.0 * 32 * 128 * (4096 * 4097 / 2)
+    return {"us": round(pms * 1e3, 1), "tflops": round(flops / (pms / 1e3) / 1e12, 1),
+            "frac_of_bf16_peak": round(flops / (pms / 1e3) / 1e12 / tf_peak, 4)}
 
 
 def graph_us(fn, reps: int = 100, inner: int = 1) -> float:
@@ -726,6 +733,17 @@ def run_reference(args):
 
 def main():
     args = parse_args()
+    if args.prefill:
+        import torch
+        import speculative_decoding_verification_packed_gb300 as svp
+        from speculative_decoding_verification_packed_gb300 import build as svp_build
+        svp_build.build()
+        torch.cuda.set_device(0)
+        _, tf_peak, kind = measured_peaks()
+        r = prefill_contrast(svp, torch.device("cuda", 0), tf_peak, reps=max(1, args.steps))
+        r.update({"workload": "prefill_4096_causal", "peak_tflops": tf_peak, "peak_kind": kind})
+        print(json.dumps(r), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
