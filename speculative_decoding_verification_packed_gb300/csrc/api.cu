@@ -23,6 +23,11 @@ svp_status margin_launch(const void *logits, int64_t row_stride, int32_t rows, i
                          float *margin, const int32_t *tokens, const int32_t *cu_slots,
                          int32_t n, int32_t *accept_len, int32_t *next_token, void *ws,
                          size_t ws_bytes, cudaStream_t stream);
+bool prefill_tc_supported(int32_t n, int32_t max_s, int32_t hq, int32_t hkv, int32_t d);
+svp_status prefill_tc_launch(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                             const int32_t *cu_seqlens, int32_t n, int32_t max_s, int32_t total_s,
+                             int32_t hq, int32_t hkv, float scale_log2, void *out, float *lse,
+                             int32_t *status, int grid, cudaStream_t stream);
 svp_status accept_launch(const int32_t *target_argmax, const int32_t *tokens,
                          const int32_t *cu_slots, int32_t n, int32_t m_cap,
                          int32_t *accept_len, int32_t *next_token, cudaStream_t stream);
@@ -424,6 +429,38 @@ svp_status svp_prefill_attn(const void *q, const void *k, const void *v,
         return SVP_EUNSUPPORTED;
     if (total_s < 0 || total_s >= (int64_t)INT32_MAX || max_s < 1)
         return SVP_EINVAL;
+    if (heads && prefill_tc_supported(n, max_s, heads->hq, heads->hkv, heads->d)) {
+        // the dedicated kernel: head_dim 128, an even number of query heads per KV head
+        if (!ws)
+            return SVP_EWORKSPACE;
+        size_t need = 0;
+        const svp_status st = svp_prefill_attn_workspace_size(n, max_s, heads, dtype, &need);
+        if (st != SVP_OK)
+            return st;
+        if (ws_bytes < need)
+            return SVP_EWORKSPACE;
+        if (n == 0 || total_s == 0)
+            return SVP_OK;
+        if (!q || !k || !v || !cu_seqlens || !out)
+            return SVP_EINVAL;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+            return SVP_EINVAL;
+        const int32_t hq = heads->hq, hkv = heads->hkv, d = heads->d;
+        CUtensorMap tq, tk, tv;
+        const uint64_t esz = 2;
+        const uint32_t box[3] = {64, 1, 128};
+        const uint64_t dq[3] = {(uint64_t)d, (uint64_t)hq, (uint64_t)total_s};
+        const uint64_t sq[2] = {d * esz, (uint64_t)hq * d * esz};
+        const uint64_t dk[3] = {(uint64_t)d, (uint64_t)hkv, (uint64_t)total_s};
+        const uint64_t sk[2] = {d * esz, (uint64_t)hkv * d * esz};
+        if (!encode_bf16(&tq, q, 3, dq, sq, box) || !encode_bf16(&tk, k, 3, dk, sk, box) ||
+            !encode_bf16(&tv, v, 3, dk, sk, box))
+            return SVP_EUNSUPPORTED;
+        const float scale = heads->scale != 0.0f ? heads->scale : 1.0f / std::sqrt((float)d);
+        return prefill_tc_launch(tq, tk, tv, cu_seqlens, n, max_s, (int32_t)total_s, hq, hkv,
+                                 scale * 1.4426950408889634f, out, lse,
+                                 static_cast<int32_t *>(ws), sm_count(), (cudaStream_t)stream);
+    }
     svp_kv kv;
     std::memset(&kv, 0, sizeof kv);   // no committed context
     return verify_impl(q, k, v, &kv, nullptr, cu_seqlens, n, (int32_t)total_s, max_s, heads,

@@ -173,6 +173,26 @@ def test_prefill_4096_sampled_heads():
                           torch.bfloat16)
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (6, 2)])
+def test_prefill_varlen_sequences(hq, hkv):
+    # several packed sequences, lengths off the 128-row tile (one shorter than a tile, one
+    # exactly a tile); G = 4 takes the dedicated kernel, G = 3 (odd) the general one
+    lens = [300, 128, 77, 1000]
+    parts = [wl.make_prefill(seed=20 + i, s=L, hq=hq, hkv=hkv, d=128) for i, L in enumerate(lens)]
+    q = torch.cat([x[0] for x in parts])
+    k = torch.cat([x[1] for x in parts])
+    v = torch.cat([x[2] for x in parts])
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    out, lse = svp.prefill_attn(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), max_s=max(lens))
+    torch.cuda.synchronize()
+    import oracle
+    n = len(lens)
+    ref_o, ref_l = oracle.attention(q, k, v, torch.zeros(n, dtype=torch.int32), cu, hkv=hkv,
+                                    scale=128 ** -0.5, k_ctx=k[:0], v_ctx=v[:0],
+                                    cu_ctx=torch.zeros(n + 1, dtype=torch.int64), threads=16)
+    compare_attention(out, lse, ref_o, ref_l, np.arange(int(cu[-1])), torch.bfloat16)
+
+
 def test_inactive_requests_and_empty_batch():
     b = wl.make_batch("budget8n_bf16", seed=7, n=4, lengths=[3, 0, 5, 0],
                       ctx_lengths=[100, 50, 0, 10], hq=8, hkv=2, d=128, poison=True)
