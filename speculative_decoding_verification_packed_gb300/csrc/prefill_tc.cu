@@ -20,7 +20,7 @@
 //   * Issue order per KV tile t: PV_0(t), S_0(t+1), PV_1(t), S_1(t+1): the softmax of one
 //     query tile runs while the tensor pipe works on the other.
 //   * The running row maximum is moved (and O_a rescaled in TMEM by its own thread) only when
-//     a tile's maximum exceeds it by 2^8; the commit that signals S_a(t) also covers PV_a(t-1),
+//     a tile's maximum exceeds it by 2^32; the commit that signals S_a(t) also covers PV_a(t-1),
 //     so O_a is stable while its thread rescales it.
 //   TMEM: S_0 / P_0 [0, 128), S_1 / P_1 [128, 256), O_0 [256, 384), O_1 [384, 512).
 #include <algorithm>
@@ -37,7 +37,7 @@ constexpr int kPfTile = 2 * kPfSub;  // [128][128] bf16
 constexpr int kPfSlots = 5;          // K / V ring slots, one tile each
 constexpr int kPfMaxSeq = 16;        // sequences per launch (tables in shared memory)
 constexpr int kPfMaxTiles = 256;     // query tiles per sequence (32K rows)
-constexpr float kPfSlack = 8.0f;     // the running maximum moves when exceeded by 2^8
+constexpr float kPfSlack = 32.0f;    // the running maximum moves when exceeded by 2^32
 constexpr int kPfOffRing = 2 * kPfTile;
 constexpr int kPfOffMisc = kPfOffRing + kPfSlots * kPfTile;
 constexpr int kPfSmem = kPfOffMisc + 1536 + 1024;   // misc region + alignment slack
@@ -79,6 +79,33 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Two fp32 values in one 64-bit register, and packed fp32 fma / add on them.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 // Item idx (in heaviest-first order) -> query tile, sequence, head pair.
@@ -350,25 +377,50 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
                     break;
                 __syncwarp();
                 tc_fence_after();
-                uint32_t sv[4][32];
+                // Keys hidden from this row (past it, or past the sequence) only occur in the
+                // diagonal tile and in the sequence's last tile; elsewhere the scores are used as
+                // they are.  Raw scores are used: the scale is positive, so the maximum of the
+                // scaled scores is the scaled maximum, and 2^(s c - m) is one fma.  One pass over
+                // the scores: P against the current reference goes to registers while the tile
+                // maximum is tracked; it is stored only if no score exceeds the reference by more
+                // than 2^32 (P then fits bf16 and the fp32 sums); otherwise (the first tile of an
+                // item, and rarely later) the reference moves and the tile is recomputed.
+                const bool full = t < it.j && (t + 1) * 128 <= it.len;
+                const int32_t kmax = full ? 127 : min(qrow, it.len - 1) - t * 128;   // last visible key
+                uint32_t pk[2][32];
+                uint64_t l2 = f32x2_pack(0.0f, 0.0f);
+#pragma unroll 1
+                for (int pass = 0; pass < 2; ++pass) {
+                    const uint64_t c2 = f32x2_pack(cl2, cl2), nm2 = f32x2_pack(-m_ref, -m_ref);
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    l2 = f32x2_pack(0.0f, 0.0f);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    tmem_ld32(ts + cc * 32, sv[cc]);
-                tmem_wait_ld();
-                // visible keys: key k of tile t is t * 128 + k <= qrow (causal, same
-                // sequence) and inside the sequence
-                const int32_t kmax = min(qrow, it.len - 1) - t * 128;   // last visible key
-                float tmax = -INFINITY;
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t sa[32], sb[32];
+                        tmem_ld32(ts + half * 64, sa);
+                        tmem_ld32(ts + half * 64 + 32, sb);
+                        tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = (cc * 32 + e <= kmax) ? __uint_as_float(sv[cc][e]) * cl2 : -INFINITY;
-                        sv[cc][e] = __float_as_uint(x);
-                        tmax = fmaxf(tmax, x);
+                        for (int e = 0; e < 32; ++e) {
+                            const int k0 = half * 64 + 2 * e;     // keys k0, k0 + 1
+                            const uint32_t r0 = e < 16 ? sa[2 * e] : sb[2 * e - 32];
+                            const uint32_t r1 = e < 16 ? sa[2 * e + 1] : sb[2 * e - 31];
+                            const float s0 = (full || k0 <= kmax) ? __uint_as_float(r0) : -INFINITY;
+                            const float s1 = (full || k0 + 1 <= kmax) ? __uint_as_float(r1) : -INFINITY;
+                            mx[(2 * e) & 3] = fmaxf(mx[(2 * e) & 3], s0);
+                            mx[(2 * e + 1) & 3] = fmaxf(mx[(2 * e + 1) & 3], s1);
+                            float y0, y1;
+                            f32x2_unpack(f32x2_fma(f32x2_pack(s0, s1), c2, nm2), y0, y1);
+                            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+                            pk[half][e] = pack_bf16x2(p0, p1);
+                            l2 = f32x2_add(l2, f32x2_pack(p0, p1));
+                        }
                     }
-                if (tmax > m_ref + kPfSlack) {
-                    // move the reference: O_a (complete up to tile t-1) and l scaled down
+                    const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cl2;
+                    if (pass == 1 || !(tmax > m_ref + kPfSlack))
+                        break;
+                    // move the reference: O_a (complete up to tile t-1) and l scaled down,
+                    // then this tile again
                     const float alpha = (m_ref == -INFINITY) ? 0.0f : fast_exp2(m_ref - tmax);
                     if (t > 0) {
 #pragma unroll 1
@@ -385,20 +437,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
                     l *= alpha;
                     m_ref = tmax;
                 }
-                // P = 2^(x - m_ref) in bf16 over the first 64 columns of S_a; l sums the
-                // rounded weights that PV uses
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int k0 = half * 64 + 2 * e;
-                        const float p0 = fast_exp2(__uint_as_float(sv[k0 >> 5][k0 & 31]) - m_ref);
-                        const float p1 = fast_exp2(__uint_as_float(sv[(k0 + 1) >> 5][(k0 + 1) & 31]) - m_ref);
-                        pk[e] = pack_bf16x2(p0, p1);
-                        l += bf16_lo(pk[e]) + bf16_hi(pk[e]);
-                    }
-                    tmem_st32(ts + half * 32, pk);
+                // P over columns [0, 64) of S_a, in bf16 (the scores there have been read)
+                tmem_st32(ts, pk[0]);
+                tmem_st32(ts + 32, pk[1]);
+                {
+                    float la, lb;
+                    f32x2_unpack(l2, la, lb);
+                    l += la + lb;
                 }
                 tmem_wait_st();
                 tc_fence_before();
