@@ -19,9 +19,10 @@
 //     order, so S_a(t+1), issued after PV_a(t), overwrites S_a only once P_a(t) has been read.
 //   * Issue order per KV tile t: PV_0(t), S_0(t+1), PV_1(t), S_1(t+1): the softmax of one
 //     query tile runs while the tensor pipe works on the other.
-//   * The running row maximum is moved (and O_a rescaled in TMEM by its own thread) only when
-//     a tile's maximum exceeds it by 2^32; the commit that signals S_a(t) also covers PV_a(t-1),
-//     so O_a is stable while its thread rescales it.
+//   * The exponent reference of a row is its maximum over the item's first KV tile; it is
+//     moved (and O_a rescaled in TMEM by its own thread) only when a later tile's row sum of
+//     2^(s - reference) exceeds 2^32, so ordinary tiles need no maximum.  The commit that
+//     signals S_a(t) also covers PV_a(t-1), so O_a is stable while its thread rescales it.
 //   TMEM: S_0 / P_0 [0, 128), S_1 / P_1 [128, 256), O_0 [256, 384), O_1 [384, 512).
 #include <algorithm>
 #include <cfloat>
@@ -37,7 +38,7 @@ constexpr int kPfTile = 2 * kPfSub;  // [128][128] bf16
 constexpr int kPfSlots = 5;          // K / V ring slots, one tile each
 constexpr int kPfMaxSeq = 16;        // sequences per launch (tables in shared memory)
 constexpr int kPfMaxTiles = 256;     // query tiles per sequence (32K rows)
-constexpr float kPfSlack = 32.0f;    // the running maximum moves when exceeded by 2^32
+constexpr float kPfSumLimit = 4294967296.0f;   // 2^32: a tile row sum above it moves the reference
 constexpr int kPfOffRing = 2 * kPfTile;
 constexpr int kPfOffMisc = kPfOffRing + kPfSlots * kPfTile;
 constexpr int kPfSmem = kPfOffMisc + 1536 + 1024;   // misc region + alignment slack
@@ -106,6 +107,68 @@ __device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b)
     uint64_t r;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
+}
+
+// Largest raw score of this thread's row in one S tile (TMEM columns ts .. ts + 127); with
+// kMasked, keys past kmax are hidden.
+template <bool kMasked>
+__device__ __forceinline__ float pf_row_max(uint32_t ts, int32_t kmax)
+{
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t sa[32], sb[32];
+        tmem_ld32(ts + half * 64, sa);
+        tmem_ld32(ts + half * 64 + 32, sb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+            const float v = __uint_as_float(e < 32 ? sa[e] : sb[e - 32]);
+            mx[e & 3] = fmaxf(mx[e & 3], (!kMasked || half * 64 + e <= kmax) ? v : -INFINITY);
+        }
+    }
+    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// P = 2^(s * cl2 - m_ref) of this thread's row in one S tile, as 64 bf16 pairs (keys 2e and
+// 2e + 1 in pk[e]), and the sum of the 128 values in fp32.
+template <bool kMasked>
+__device__ __forceinline__ float pf_row_exp(uint32_t ts, int32_t kmax, float cl2, float m_ref,
+                                            uint32_t (&pk)[64])
+{
+    const uint64_t c2 = f32x2_pack(cl2, cl2), nm2 = f32x2_pack(-m_ref, -m_ref);
+    uint64_t acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        acc[i] = f32x2_pack(0.0f, 0.0f);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t sa[32], sb[32];
+        tmem_ld32(ts + half * 64, sa);
+        tmem_ld32(ts + half * 64 + 32, sb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int k0 = half * 64 + 2 * e;
+            float s0 = __uint_as_float(e < 16 ? sa[2 * e] : sb[2 * e - 32]);
+            float s1 = __uint_as_float(e < 16 ? sa[2 * e + 1] : sb[2 * e - 31]);
+            if (kMasked) {
+                s0 = k0 <= kmax ? s0 : -INFINITY;
+                s1 = k0 + 1 <= kmax ? s1 : -INFINITY;
+            }
+            float y0, y1;
+            f32x2_unpack(f32x2_fma(f32x2_pack(s0, s1), c2, nm2), y0, y1);
+            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+            pk[half * 32 + e] = pack_bf16x2(p0, p1);
+            acc[e & 3] = f32x2_add(acc[e & 3], f32x2_pack(p0, p1));
+        }
+    }
+    float a0, a1, b0, b1, c0, c1, d0, d1;
+    f32x2_unpack(acc[0], a0, a1);
+    f32x2_unpack(acc[1], b0, b1);
+    f32x2_unpack(acc[2], c0, c1);
+    f32x2_unpack(acc[3], d0, d1);
+    return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
 }
 
 // Item idx (in heaviest-first order) -> query tile, sequence, head pair.
@@ -373,78 +436,57 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
             const int32_t qrow = it.j * 128 + r;               // row index within the sequence
             float m_ref = -INFINITY, l = 0.0f;
             for (int32_t t = 0; t <= it.j; ++t, ++it_g) {
-                if (!(ok = mbar_wait(bar_sfull(a), it_g & 1u, abort_flag)))
+                // warp-uniform outcome: the TMEM accesses below are warp-collective
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_sfull(a), it_g & 1u, abort_flag))))
                     break;
-                __syncwarp();
                 tc_fence_after();
                 // Keys hidden from this row (past it, or past the sequence) only occur in the
                 // diagonal tile and in the sequence's last tile; elsewhere the scores are used as
                 // they are.  Raw scores are used: the scale is positive, so the maximum of the
-                // scaled scores is the scaled maximum, and 2^(s c - m) is one fma.  One pass over
-                // the scores: P against the current reference goes to registers while the tile
-                // maximum is tracked; it is stored only if no score exceeds the reference by more
-                // than 2^32 (P then fits bf16 and the fp32 sums); otherwise (the first tile of an
-                // item, and rarely later) the reference moves and the tile is recomputed.
-                const bool full = t < it.j && (t + 1) * 128 <= it.len;
-                const int32_t kmax = full ? 127 : min(qrow, it.len - 1) - t * 128;   // last visible key
-                uint32_t pk[2][32];
-                uint64_t l2 = f32x2_pack(0.0f, 0.0f);
+                // scaled scores is the scaled maximum, and 2^(s c - m) is one fma.  P is taken
+                // against the reference m_ref in one pass over the scores; the reference is set to
+                // the row maximum on the item's first tile, and moved later only when a tile's row
+                // sum exceeds 2^32 (some score then lies more than 2^25 above it): O_a and l are
+                // rescaled and the tile is recomputed against the larger of the two.
+                const bool masked = !(t < it.j && (t + 1) * 128 <= it.len);
+                const int32_t kmax = masked ? min(qrow, it.len - 1) - t * 128 : 127;   // last visible key
+                uint32_t pk[64];
+                float tsum;
+                bool move = (t == 0);
 #pragma unroll 1
-                for (int pass = 0; pass < 2; ++pass) {
-                    const uint64_t c2 = f32x2_pack(cl2, cl2), nm2 = f32x2_pack(-m_ref, -m_ref);
-                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                    l2 = f32x2_pack(0.0f, 0.0f);
+                for (;;) {
+                    if (move) {
+                        // (m_ref is -inf on the first tile; later it only grows)
+                        const float tmax = fmaxf(m_ref, (masked ? pf_row_max<true>(ts, kmax)
+                                                                : pf_row_max<false>(ts, kmax)) * cl2);
+                        if (t > 0) {
+                            const float alpha = fast_exp2(m_ref - tmax);
+#pragma unroll 1
+                            for (int cc = 0; cc < 4; ++cc) {
+                                uint32_t ov[32];
+                                tmem_ld32(to + cc * 32, ov);
+                                tmem_wait_ld();
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t sa[32], sb[32];
-                        tmem_ld32(ts + half * 64, sa);
-                        tmem_ld32(ts + half * 64 + 32, sb);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int k0 = half * 64 + 2 * e;     // keys k0, k0 + 1
-                            const uint32_t r0 = e < 16 ? sa[2 * e] : sb[2 * e - 32];
-                            const uint32_t r1 = e < 16 ? sa[2 * e + 1] : sb[2 * e - 31];
-                            const float s0 = (full || k0 <= kmax) ? __uint_as_float(r0) : -INFINITY;
-                            const float s1 = (full || k0 + 1 <= kmax) ? __uint_as_float(r1) : -INFINITY;
-                            mx[(2 * e) & 3] = fmaxf(mx[(2 * e) & 3], s0);
-                            mx[(2 * e + 1) & 3] = fmaxf(mx[(2 * e + 1) & 3], s1);
-                            float y0, y1;
-                            f32x2_unpack(f32x2_fma(f32x2_pack(s0, s1), c2, nm2), y0, y1);
-                            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-                            pk[half][e] = pack_bf16x2(p0, p1);
-                            l2 = f32x2_add(l2, f32x2_pack(p0, p1));
+                                for (int e = 0; e < 32; ++e)
+                                    ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                                tmem_st32(to + cc * 32, ov);
+                            }
+                            l *= alpha;
                         }
+                        m_ref = tmax;
                     }
-                    const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cl2;
-                    if (pass == 1 || !(tmax > m_ref + kPfSlack))
+                    tsum = masked ? pf_row_exp<true>(ts, kmax, cl2, m_ref, pk)
+                                  : pf_row_exp<false>(ts, kmax, cl2, m_ref, pk);
+                    // tcgen05.ld / st are warp-collective (.sync.aligned): the warp takes the
+                    // move together when any of its rows needs it (NaN sums included)
+                    if (move || !__any_sync(0xffffffffu, !(tsum <= kPfSumLimit)))
                         break;
-                    // move the reference: O_a (complete up to tile t-1) and l scaled down,
-                    // then this tile again
-                    const float alpha = (m_ref == -INFINITY) ? 0.0f : fast_exp2(m_ref - tmax);
-                    if (t > 0) {
-#pragma unroll 1
-                        for (int cc = 0; cc < 4; ++cc) {
-                            uint32_t ov[32];
-                            tmem_ld32(to + cc * 32, ov);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                            tmem_st32(to + cc * 32, ov);
-                        }
-                    }
-                    l *= alpha;
-                    m_ref = tmax;
+                    move = true;
                 }
                 // P over columns [0, 64) of S_a, in bf16 (the scores there have been read)
-                tmem_st32(ts, pk[0]);
-                tmem_st32(ts + 32, pk[1]);
-                {
-                    float la, lb;
-                    f32x2_unpack(l2, la, lb);
-                    l += la + lb;
-                }
+                tmem_st32(ts, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+                tmem_st32(ts + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+                l += tsum;
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -454,9 +496,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
             if (!ok)
                 break;
             // ---- epilogue: O_a complete after the item's last PV_a
-            if (!(ok = mbar_wait(bar_oready(a), nitem & 1u, abort_flag)))
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_oready(a), nitem & 1u, abort_flag))))
                 break;
-            __syncwarp();
             tc_fence_after();
             const float inv = 1.0f / l;
             const bool live = qrow < it.len;
@@ -493,8 +534,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1)
+    if (warp == 1) {
+        __syncwarp();
         tmem_dealloc(tmem, 512);
+    }
 }
 
 // ------------------------------------------------------------------------ host side

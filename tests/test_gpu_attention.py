@@ -173,6 +173,26 @@ def test_prefill_4096_sampled_heads():
                           torch.bfloat16)
 
 
+def test_prefill_scores_jumping_between_tiles():
+    # Every query leans on the all-ones direction and the keys are shifted along it by 0, 3
+    # and 6 every two 128-key tiles, so rows that see tile 2 or tile 4 meet scores about 50
+    # (in log2 units) above everything before: the exponent reference must move in the middle
+    # of the row, with O and the row sum rescaled.  Exact softmax in the oracle.
+    s = 700
+    q, k, v = wl.make_prefill(seed=4, s=s, hq=4, hkv=2, d=128)
+    shift = torch.tensor([0.0, 0.0, 3.0, 3.0, 6.0, 6.0]).repeat_interleave(128)[:s]
+    q = (q.float() + 1.0).to(torch.bfloat16)
+    k = (k.float() + shift[:, None, None]).to(torch.bfloat16)
+    cu = torch.tensor([0, s], dtype=torch.int32)
+    out, lse = svp.prefill_attn(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), max_s=s)
+    torch.cuda.synchronize()
+    import oracle
+    ref_o, ref_l = oracle.attention(q, k, v, torch.zeros(1, dtype=torch.int32), cu, hkv=2,
+                                    scale=128 ** -0.5, k_ctx=k[:0], v_ctx=v[:0],
+                                    cu_ctx=torch.zeros(2, dtype=torch.int64), threads=16)
+    compare_attention(out, lse, ref_o, ref_l, np.arange(s), torch.bfloat16)
+
+
 @pytest.mark.parametrize("hq,hkv", [(8, 2), (6, 2)])
 def test_prefill_varlen_sequences(hq, hkv):
     # several packed sequences, lengths off the 128-row tile (one shorter than a tile, one
