@@ -13,10 +13,12 @@ A step is one pass of the hot path over one batch of the workload:
 The metric is verified candidate rows per second (rows = packed live rows M_live).
 Inputs are resident in HBM when the timed region starts; consecutive steps rotate over
 several independent input sets whose total footprint exceeds twice the L2 size, so a
-step never finds its KV stream in L2.  Each launch of a step is replayed from a CUDA
-graph captured once per input set (the C-ABI calls are capture-safe, as a serving step
-would replay them), so the timed region holds no host work; CUDA events around every
-launch give the per-kernel durations used for the roofline.  Rank 0 prints one JSON line.
+step never finds its KV stream in L2.  Each step is one replay of a CUDA graph of its
+launches, captured per input set (the C-ABI calls are capture-safe, as a serving loop
+would replay its verify step), so the timed region holds no host work.  Timing events
+recorded inside the graph around every launch give the per-kernel durations used for the
+roofline: 16 copies of each graph are cycled, and the durations are those of the last
+16 x sets steps of the timed region.  Rank 0 prints one JSON line.
 
 --impl reference times the fp64 CPU oracle (the reference arm of this repository) on a
 bounded sample of the same workload on the host cores.
@@ -242,21 +244,34 @@ def n_sets_for(b0) -> int:
     return max(1, min(8, math.ceil(2 * L2_BYTES / per) + 1)) if per < 4 * L2_BYTES else 1
 
 
-def capture_step(plan, stream):
-    """One CUDA graph per launch of the step (replayed in order inside the timed loop)."""
+GRAPH_COPIES = 16   # step graphs per input set: the last replays of the timed region
+
+
+def capture_step(plan, stream, copies=GRAPH_COPIES):
+    """The whole step as one CUDA graph (the launches in order, as a serving loop replays
+    its verify step), with a timing event recorded inside the graph before and after every
+    launch.  `copies` graphs are captured, each with its own events, so that the timed
+    loop can cycle through them and every copy keeps the durations of its last replay."""
     import torch
     with torch.cuda.stream(stream):
         for _, fn in plan:
             fn()                      # first use: workspace signature, lazy init
     torch.cuda.synchronize()
-    graphs = []
-    for name, fn in plan:
+    out = []
+    for _ in range(copies):
         g = torch.cuda.CUDAGraph()
+        evs = []
         with torch.cuda.graph(g, stream=stream):
-            fn()
-        graphs.append((name, g))
+            for name, fn in plan:
+                e0 = torch.cuda.Event(enable_timing=True, external=True)
+                e1 = torch.cuda.Event(enable_timing=True, external=True)
+                e0.record()
+                fn()
+                e1.record()
+                evs.append((name, e0, e1))
+        out.append((g, evs))
     torch.cuda.synchronize()
-    return graphs
+    return out
 
 
 def launch_dist(times_ms):
@@ -270,45 +285,46 @@ def launch_dist(times_ms):
 
 
 def timed_run(sets, steps, warmup, svp, tile_mode=None, clocks=None, dist_out=None):
-    """K steps rotating over the input sets, each step replayed from captured graphs
-    (no host work inside the timed region); per-launch device times from events
-    recorded on the stream around each launch."""
+    """K steps rotating over the input sets, each step one replay of a captured step graph
+    (no host work inside the timed region).  ms per step from events on the stream around
+    the K replays; per-launch device times from the events inside the graphs, i.e. from
+    the last replay of every graph copy (the last copies x sets steps of the region)."""
     import torch
     stream = torch.cuda.current_stream()
     plans = [build_step(b, svp, tile_mode)[0] for b in sets]
-    graphs = [capture_step(pl, torch.cuda.Stream()) for pl in plans]
+    cap = torch.cuda.Stream()
+    graphs = [capture_step(pl, cap) for pl in plans]
+    nsets = len(graphs)
+    pick = lambda s: graphs[s % nsets][(s // nsets) % GRAPH_COPIES]
     if clocks:
         clocks.start()          # sampling spans the warm-up and the timed region
         time.sleep(0.2)
     for w in range(warmup):
-        for _, g in graphs[w % len(graphs)]:
-            g.replay()
+        pick(w)[0].replay()
     torch.cuda.synchronize()
-    nl = len(graphs[0])
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(nl)] for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     t0.record(stream)
     for s in range(steps):
-        for li, (_, g) in enumerate(graphs[s % len(graphs)]):
-            ev[s][li][0].record(stream)
-            g.replay()
-            ev[s][li][1].record(stream)
+        pick(s)[0].replay()
     t1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     clk = clocks.stop() if clocks else None
     total_ms = t0.elapsed_time(t1)
-    per_launch = [statistics.mean(ev[s][li][0].elapsed_time(ev[s][li][1]) for s in range(steps))
-                  for li in range(nl)]
-    names = [n for n, _ in graphs[0]]
+    names = [n for n, _ in plans[0]]
+    replayed = {(s % nsets, (s // nsets) % GRAPH_COPIES) for s in range(steps)}
+    samples = [[] for _ in names]
+    for (si, ci) in sorted(replayed):
+        for li, (_, e0, e1) in enumerate(graphs[si][ci][1]):
+            samples[li].append(e0.elapsed_time(e1))
+    per_launch = [statistics.mean(x) for x in samples]
     if dist_out is not None:
         for li, name in enumerate(names):
-            dist_out[name] = launch_dist([ev[s][li][0].elapsed_time(ev[s][li][1]) for s in range(steps)])
-    return total_ms, dict(zip(names, per_launch)), clk, wall, steps * nl
+            dist_out[name] = launch_dist(samples[li])
+    return total_ms, dict(zip(names, per_launch)), clk, wall, steps * len(names)
 
 
 def e2e_run(sets, steps, warmup, svp):

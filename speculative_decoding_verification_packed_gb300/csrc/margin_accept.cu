@@ -19,7 +19,7 @@
 //     on a strictly larger value (the lane's first occurrence of its maximum).
 //   * Triples merge by warp shuffles; the merge is commutative and associative (ties:
 //     lowest index), so results do not depend on arrival order.
-//   * The warp that finishes the last chunk of a row (atomic ticket, no waiting)
+//   * The warp that finishes the last chunk of a row (acquire-release ticket, no waiting)
 //     finalises the row; in the fused kernel the warp that finalises the last row of a
 //     request then runs the greedy acceptance for that request, all candidates at once
 //     (lane l compares candidate l, the first mismatch by ballot).  Tickets, partials and
@@ -284,14 +284,14 @@ __global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
         int last = 0;
         if (lane == 0) {
             a.partial[row * a.chunks_per_row + ch] = t;
-            __threadfence();
-            last = atomicAdd(a.row_ticket + row, 1) == a.chunks_per_row - 1;
+            last = ticket_add_acq_rel(a.row_ticket + row, 1) == a.chunks_per_row - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (!last)
             continue;
-        // last chunk of this row: merge its partials (lane-parallel) and clear them
-        __threadfence();
+        // last chunk of this row: merge its partials (lane-parallel) and clear them; lane 0's
+        // acquire orders the other lanes' reads through the warp barrier
+        __syncwarp();
         Top2 *pp = a.partial + row * a.chunks_per_row;
         Top2 r = top2_identity();
         for (int32_t k = lane; k < a.chunks_per_row; k += 32) {
@@ -312,11 +312,9 @@ __global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
             if (a.margin) a.margin[row] = __fsub_rn(r.v1, r.v2);
             if (a.cu_slots) {
                 a.row_argmax[row] = r.i1;
-                __threadfence();
                 const int32_t i = owner_of_row(a.cu_slots, a.n, (int32_t)row);
                 const int32_t k = __ldg(a.cu_slots + i + 1) - __ldg(a.cu_slots + i);
-                if (atomicAdd(a.req_ticket + i, 1) == k - 1) {
-                    __threadfence();
+                if (ticket_add_acq_rel(a.req_ticket + i, 1) == k - 1) {
                     a.req_ticket[i] = 0;
                     fin = i;
                 }
@@ -324,7 +322,7 @@ __global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
         }
         fin = __shfl_sync(0xffffffffu, fin, 0);
         if (fin >= 0) {
-            __syncwarp();   // lane 0's acquire (ticket + fence) orders the other lanes' reads
+            __syncwarp();   // lane 0's acquire on the request ticket orders the other lanes' reads
             finish_request(a, fin, lane);
         }
     }

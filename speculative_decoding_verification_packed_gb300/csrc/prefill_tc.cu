@@ -141,27 +141,26 @@ __device__ __forceinline__ float pf_row_exp(uint32_t ts, int32_t kmax, float cl2
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         acc[i] = f32x2_pack(0.0f, 0.0f);
+    // all 128 scores in one round trip; each register dies as its P value is packed
+    uint32_t sv[4][32];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        uint32_t sa[32], sb[32];
-        tmem_ld32(ts + half * 64, sa);
-        tmem_ld32(ts + half * 64 + 32, sb);
-        tmem_wait_ld();
+    for (int q = 0; q < 4; ++q)
+        tmem_ld32(ts + q * 32, sv[q]);
+    tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const int k0 = half * 64 + 2 * e;
-            float s0 = __uint_as_float(e < 16 ? sa[2 * e] : sb[2 * e - 32]);
-            float s1 = __uint_as_float(e < 16 ? sa[2 * e + 1] : sb[2 * e - 31]);
-            if (kMasked) {
-                s0 = k0 <= kmax ? s0 : -INFINITY;
-                s1 = k0 + 1 <= kmax ? s1 : -INFINITY;
-            }
-            float y0, y1;
-            f32x2_unpack(f32x2_fma(f32x2_pack(s0, s1), c2, nm2), y0, y1);
-            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-            pk[half * 32 + e] = pack_bf16x2(p0, p1);
-            acc[e & 3] = f32x2_add(acc[e & 3], f32x2_pack(p0, p1));
+    for (int e = 0; e < 64; ++e) {
+        const int k0 = 2 * e;
+        float s0 = __uint_as_float(sv[k0 >> 5][k0 & 31]);
+        float s1 = __uint_as_float(sv[k0 >> 5][(k0 & 31) + 1]);
+        if (kMasked) {
+            s0 = k0 <= kmax ? s0 : -INFINITY;
+            s1 = k0 + 1 <= kmax ? s1 : -INFINITY;
         }
+        float y0, y1;
+        f32x2_unpack(f32x2_fma(f32x2_pack(s0, s1), c2, nm2), y0, y1);
+        const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+        pk[e] = pack_bf16x2(p0, p1);
+        acc[e & 3] = f32x2_add(acc[e & 3], f32x2_pack(p0, p1));
     }
     float a0, a1, b0, b1, c0, c1, d0, d1;
     f32x2_unpack(acc[0], a0, a1);

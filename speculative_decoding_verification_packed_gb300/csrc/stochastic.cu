@@ -209,13 +209,11 @@ __global__ void __launch_bounds__(kStThreads1, 4) st_rowstat_kernel(const StPara
             continue;
         }
         int last = 0;
-        if (lane == 0) {
-            __threadfence();
-            last = atomicAdd(p.tickets + r, 1) == p.chunks - 1;
-        }
+        if (lane == 0)
+            last = ticket_add_acq_rel(p.tickets + r, 1) == p.chunks - 1;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
-            __threadfence();
+            __syncwarp();   // lane 0's acquire orders the other lanes' reads of the partials
             float2 t = make_float2(-INFINITY, 0.0f);
             for (int q = lane; q < p.chunks; q += 32)
                 t = st_merge(t, __ldcg(p.partial + (int64_t)r * p.chunks + q), p.c);

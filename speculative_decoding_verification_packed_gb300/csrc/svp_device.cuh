@@ -440,6 +440,17 @@ inline cudaError_t set_smem_limit_once(K kernel, int bytes, std::atomic<uint64_t
     return e;
 }
 
+// Ticket counter increment at gpu scope with acquire-release semantics: the writes this
+// thread made before it are visible to whoever later reads the count it produced, and this
+// thread's later reads see the writes that the earlier incrementers made before theirs.
+// Other lanes of the warp order their reads after it with __syncwarp().
+__device__ __forceinline__ int32_t ticket_add_acq_rel(int32_t *p, int32_t v)
+{
+    int32_t r;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+    return r;
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int32_t bits)
 {
     if (status)
