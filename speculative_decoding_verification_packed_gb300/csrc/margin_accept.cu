@@ -19,12 +19,15 @@
 //     on a strictly larger value (the lane's first occurrence of its maximum).
 //   * Triples merge by warp shuffles; the merge is commutative and associative (ties:
 //     lowest index), so results do not depend on arrival order.
-//   * The warp that finishes the last chunk of a row (acquire-release ticket, no waiting)
-//     finalises the row; in the fused kernel the warp that finalises the last row of a
-//     request then runs the greedy acceptance for that request, all candidates at once
-//     (lane l compares candidate l, the first mismatch by ballot).  Tickets, partials and
-//     per-row argmaxes are cleared by their last reader, so the workspace is all zero
-//     again after every call and can serve calls of any size.
+//   * Draft rows (no acceptance): the warp that delivers the last chunk of a row (one
+//     acquire-release ticket per row, no waiting) merges the row's chunk triples.
+//   * Fused margin + accept: the ticket is per request and counts the chunks of all its
+//     rows, so the warp that delivers the request's last chunk merges every row of the
+//     request (four lanes per row, eight rows per pass), writes the row outputs and runs
+//     the greedy acceptance on the row argmaxes it holds: one ticket and one read-back on
+//     the tail instead of a row level and a request level.  Tickets and triples are
+//     cleared by their last reader, so the workspace is all zero again after every call
+//     and can serve calls of any size.
 #include <cfloat>
 #include <climits>
 #include <cuda_bf16.h>
@@ -85,6 +88,14 @@ __device__ __forceinline__ Top2 top2_warp_merge(Top2 t)
     return t;
 }
 
+// A chunk's triple as stored in the workspace: 16 bytes, read back with one vector load.
+struct alignas(16) Top2Part {
+    float v1;
+    float v2;
+    int32_t i1;
+    int32_t pad;
+};
+
 struct MarginArgs {
     const void *logits;
     int64_t row_stride;      // elements
@@ -101,7 +112,7 @@ struct MarginArgs {
     int32_t *status;
     int32_t *row_ticket;     // [rows]
     int32_t *row_argmax;     // [rows]
-    Top2 *partial;           // [rows * chunks_per_row]
+    Top2Part *partial;       // [rows * chunks_per_row]
     // fused acceptance (cu_slots == nullptr: margin only)
     const int32_t *tokens;
     const int32_t *cu_slots;
@@ -113,20 +124,6 @@ struct MarginArgs {
 
 constexpr int kMarginThreads = 256;      // 8 independent warps per CTA
 constexpr int kMarginBatch = 8;          // 16-byte loads in flight per lane
-
-// Which request owns packed row r (cu_slots non-decreasing, validated by the caller).
-__device__ __forceinline__ int32_t owner_of_row(const int32_t *cu, int32_t n, int32_t r)
-{
-    int32_t lo = 0, hi = n;   // the largest i < n with cu[i] <= r
-    while (hi - lo > 1) {
-        const int32_t mid = (lo + hi) >> 1;
-        if (__ldg(cu + mid) <= r)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    return lo;
-}
 
 template <bool kBf16>
 __device__ __forceinline__ float load_elem(const MarginArgs &a, int64_t row, int32_t e)
@@ -224,30 +221,85 @@ __device__ __forceinline__ Top2 scan_chunk_warp(const MarginArgs &a, int64_t row
     return t;
 }
 
-// Greedy acceptance of request i by one warp, once every row argmax is in: lane l compares
-// candidate j0 + l with the argmax of the row before it, and the first mismatch (ballot)
-// ends the accepted prefix.
-__device__ void finish_request(const MarginArgs &a, int32_t i, int lane)
+__device__ __forceinline__ Top2 load_part(const Top2Part *p)
 {
-    const int32_t off = __ldcg(a.cu_slots + i);
-    const int32_t k = __ldcg(a.cu_slots + i + 1) - off;
-    int32_t acc = k - 1;
-    for (int32_t j0 = 1; j0 < k; j0 += 32) {
-        const int32_t j = j0 + lane;
-        const bool miss = j < k && __ldg(a.tokens + off + j) != __ldcg(a.row_argmax + off + j - 1);
-        const uint32_t m = __ballot_sync(0xffffffffu, miss);
-        if (m) {
-            acc = j0 + __ffs(m) - 2;
-            break;
+    const int4 q = __ldcg(reinterpret_cast<const int4 *>(p));
+    return Top2{__int_as_float(q.x), __int_as_float(q.y), q.z};
+}
+
+// Request i (packed rows off .. off + k - 1) once the chunks of all its rows are in: one warp
+// merges every row's chunk triples (four lanes per row, eight rows per pass, each lane's
+// triples loaded together), writes the row outputs, and runs the greedy acceptance on the
+// row argmaxes as they come: row j's argmax is compared with draft token j + 1, and the
+// first mismatch ends the accepted prefix.  The triples it read are cleared.
+__device__ void finish_request(const MarginArgs &a, int32_t i, int32_t off, int32_t k, int lane)
+{
+    const int32_t cpr = a.chunks_per_row;
+    const int sub = lane & 3, g = lane >> 2;     // quarter and row of this lane within a pass
+    int32_t acc = -1, nxt = -1;                   // decided: accepted drafts, successor token
+    for (int32_t j0 = 0; j0 < k; j0 += 8) {
+        const int32_t j = j0 + g;                 // request row of this lane
+        const bool live = j < k;
+        const int32_t tok = live && j + 1 < k ? __ldg(a.tokens + off + j + 1) : 0;
+        Top2 r = top2_identity();
+        if (live) {
+            Top2Part *pp = a.partial + (int64_t)(off + j) * cpr;
+            for (int32_t c0 = sub; c0 < cpr; c0 += 32) {       // one pass while cpr <= 32
+                Top2 u[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    u[q] = c0 + 4 * q < cpr ? load_part(pp + c0 + 4 * q) : top2_identity();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    // chunks in increasing order within the lane: ties keep the lowest index
+                    r = top2_merge(r, u[q]);
+                    if (c0 + 4 * q < cpr)
+                        *reinterpret_cast<int4 *>(pp + c0 + 4 * q) = make_int4(0, 0, 0, 0);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {       // the row's four lanes
+            Top2 v;
+            v.v1 = __shfl_xor_sync(0xffffffffu, r.v1, o);
+            v.v2 = __shfl_xor_sync(0xffffffffu, r.v2, o);
+            v.i1 = __shfl_xor_sync(0xffffffffu, r.i1, o);
+            r = top2_merge(r, v);
+        }
+        const int64_t row = off + j;
+        if (live && sub == 0) {
+            if (a.top1_idx) a.top1_idx[row] = r.i1;
+            if (a.top1) a.top1[row] = r.v1;
+            if (a.top2) a.top2[row] = r.v2;
+            if (a.margin) a.margin[row] = __fsub_rn(r.v1, r.v2);
+        }
+        if (acc < 0) {
+            // row j ends the prefix when it is the last row or draft j + 1 differs
+            const bool stop = live && (j + 1 == k || tok != r.i1);
+            const uint32_t m = __ballot_sync(0xffffffffu, stop && sub == 0);
+            if (m) {
+                const int src = __ffs(m) - 1;
+                acc = j0 + (src >> 2);
+                nxt = __shfl_sync(0xffffffffu, r.i1, src);
+            }
         }
     }
     if (lane == 0) {
         a.accept_len[i] = 1 + acc;
-        a.next_token[i] = __ldcg(a.row_argmax + off + acc);
+        a.next_token[i] = nxt;
     }
-    __syncwarp();
-    for (int32_t j = lane; j < k; j += 32)   // the workspace returns to zero
-        a.row_argmax[off + j] = 0;
+}
+
+// Which request owns packed row r: cu_slots non-decreasing (validated), so it is the number
+// of requests 1 .. n-1 that start at or before r (empty requests own no rows).
+__device__ __forceinline__ int32_t owner_of_row_warp(const int32_t *cu, int32_t n, int32_t r, int lane)
+{
+    int32_t cnt = 0;
+    for (int32_t l0 = 1; l0 < n; l0 += 32) {
+        const int32_t l = l0 + lane;
+        cnt += __popc(__ballot_sync(0xffffffffu, l < n && __ldg(cu + l) <= r));
+    }
+    return cnt;
 }
 
 template <bool kBf16>
@@ -281,9 +333,29 @@ __global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
         const int32_t c0 = ch * a.chunk;
         const int32_t c1 = min(a.vocab, c0 + a.chunk);
         Top2 t = top2_warp_merge(scan_chunk_warp<kBf16>(a, row, c0, c1, lane));
+        if (a.cu_slots) {
+            // fused: the warp that delivers the last chunk of the last row of a request
+            // finishes the whole request (acquire-release ticket over its chunks)
+            const int32_t i = owner_of_row_warp(a.cu_slots, a.n, (int32_t)row, lane);
+            const int32_t off = __ldg(a.cu_slots + i);
+            const int32_t k = __ldg(a.cu_slots + i + 1) - off;
+            int last = 0;
+            if (lane == 0) {
+                a.partial[row * a.chunks_per_row + ch] = Top2Part{t.v1, t.v2, t.i1, 0};
+                last = ticket_add_acq_rel(a.req_ticket + i, 1) == k * a.chunks_per_row - 1;
+                if (last)
+                    a.req_ticket[i] = 0;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __syncwarp();   // lane 0's acquire orders the other lanes' reads
+                finish_request(a, i, off, k, lane);
+            }
+            continue;
+        }
         int last = 0;
         if (lane == 0) {
-            a.partial[row * a.chunks_per_row + ch] = t;
+            a.partial[row * a.chunks_per_row + ch] = Top2Part{t.v1, t.v2, t.i1, 0};
             last = ticket_add_acq_rel(a.row_ticket + row, 1) == a.chunks_per_row - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
@@ -292,38 +364,19 @@ __global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
         // last chunk of this row: merge its partials (lane-parallel) and clear them; lane 0's
         // acquire orders the other lanes' reads through the warp barrier
         __syncwarp();
-        Top2 *pp = a.partial + row * a.chunks_per_row;
+        Top2Part *pp = a.partial + row * a.chunks_per_row;
         Top2 r = top2_identity();
         for (int32_t k = lane; k < a.chunks_per_row; k += 32) {
-            Top2 u;
-            u.v1 = __ldcg(&pp[k].v1);
-            u.v2 = __ldcg(&pp[k].v2);
-            u.i1 = __ldcg(&pp[k].i1);
-            r = top2_merge(r, u);
-            pp[k] = Top2{0.0f, 0.0f, 0};
+            r = top2_merge(r, load_part(pp + k));
+            *reinterpret_cast<int4 *>(pp + k) = make_int4(0, 0, 0, 0);
         }
         r = top2_warp_merge(r);
-        int32_t fin = -1;   // request whose last row this is
         if (lane == 0) {
             a.row_ticket[row] = 0;
             if (a.top1_idx) a.top1_idx[row] = r.i1;
             if (a.top1) a.top1[row] = r.v1;
             if (a.top2) a.top2[row] = r.v2;
             if (a.margin) a.margin[row] = __fsub_rn(r.v1, r.v2);
-            if (a.cu_slots) {
-                a.row_argmax[row] = r.i1;
-                const int32_t i = owner_of_row(a.cu_slots, a.n, (int32_t)row);
-                const int32_t k = __ldg(a.cu_slots + i + 1) - __ldg(a.cu_slots + i);
-                if (ticket_add_acq_rel(a.req_ticket + i, 1) == k - 1) {
-                    a.req_ticket[i] = 0;
-                    fin = i;
-                }
-            }
-        }
-        fin = __shfl_sync(0xffffffffu, fin, 0);
-        if (fin >= 0) {
-            __syncwarp();   // lane 0's acquire on the request ticket orders the other lanes' reads
-            finish_request(a, fin, lane);
         }
     }
 
@@ -395,7 +448,7 @@ static MarginPlan margin_plan(int32_t rows, int32_t vocab, int32_t n)
     p.off_row_ticket = o; o = al(o + sizeof(int32_t) * (size_t)rows);
     p.off_row_argmax = o; o = al(o + sizeof(int32_t) * (size_t)rows);
     p.off_req_ticket = o; o = al(o + sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
-    p.off_partial = o; o = al(o + sizeof(Top2) * (size_t)rows * p.chunks_per_row);
+    p.off_partial = o; o = al(o + sizeof(Top2Part) * (size_t)rows * p.chunks_per_row);
     p.bytes = o;
     return p;
 }
@@ -447,7 +500,7 @@ svp_status margin_launch(const void *logits, int64_t row_stride, int32_t rows, i
     a.row_ticket = reinterpret_cast<int32_t *>(w + p.off_row_ticket);
     a.row_argmax = reinterpret_cast<int32_t *>(w + p.off_row_argmax);
     a.req_ticket = reinterpret_cast<int32_t *>(w + p.off_req_ticket);
-    a.partial = reinterpret_cast<Top2 *>(w + p.off_partial);
+    a.partial = reinterpret_cast<Top2Part *>(w + p.off_partial);
     a.tokens = tokens;
     a.cu_slots = cu_slots;
     a.n = n;
