@@ -253,6 +253,9 @@ def capture_step(plan, stream, copies=GRAPH_COPIES):
     launch.  `copies` graphs are captured, each with its own events, so that the timed
     loop can cycle through them and every copy keeps the durations of its last replay."""
     import torch
+    # the workspaces were cleared on the default stream; the capture stream is non-blocking,
+    # so the first calls below must not start before those clears are done
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for _, fn in plan:
             fn()                      # first use: workspace signature, lazy init

@@ -193,7 +193,11 @@ def _stream(stream) -> int:
 
 
 class Workspace:
-    """Device scratch for one entry point, zeroed once at creation (svp_workspace_init)."""
+    """Device scratch for one entry point, zeroed once at creation (svp_workspace_init).
+
+    The clear is enqueued on ``stream`` (default: the current stream).  A call on another
+    stream must be ordered after it (the same stream, a synchronize, or an event): torch's
+    side streams do not wait for the default stream."""
 
     def __init__(self, nbytes: int, device=None, stream=None):
         self.nbytes = max(int(nbytes), 256)
