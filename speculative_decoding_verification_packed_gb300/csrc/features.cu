@@ -328,23 +328,29 @@ __device__ __forceinline__ bool ft_scan_bf16(const FtParams &p, int64_t rowb, in
             }
             ft_stat_rebase(st, ft_hmax(b2));
             const float ml = st.m * kFtL2e;
-            float s0 = 0.0f, s1 = 0.0f, t0 = 0.0f, t1 = 0.0f;
+            // both values of a packed pair at once: d = z log2 e - m log2 e by one packed fma,
+            // the sum and the weighted sum by one packed add and one packed fma
+            const uint64_t l2e2 = f32x2_pack(kFtL2e, kFtL2e), nml2 = f32x2_pack(-ml, -ml);
+            uint64_t s2 = f32x2_pack(0.0f, 0.0f), t2 = s2;
 #pragma unroll
             for (int q = 0; q < kFtLoads; ++q) {
                 const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t c = bf16x2_max(w[k], kFtLow2);
-                    const float d0 = fmaf(bf16_lo(c), kFtL2e, -ml), d1 = fmaf(bf16_hi(c), kFtL2e, -ml);
-                    const float e0 = fast_exp2(d0), e1 = fast_exp2(d1);
-                    s0 += e0;
-                    s1 += e1;
-                    t0 = fmaf(e0, d0, t0);
-                    t1 = fmaf(e1, d1, t1);
+                    const uint64_t d2 = f32x2_fma(f32x2_pack(bf16_lo(c), bf16_hi(c)), l2e2, nml2);
+                    float d0, d1;
+                    f32x2_unpack(d2, d0, d1);
+                    const uint64_t e2 = f32x2_pack(fast_exp2(d0), fast_exp2(d1));
+                    s2 = f32x2_add(s2, e2);
+                    t2 = f32x2_fma(e2, d2, t2);
                 }
             }
-            st.s += s0 + s1;
-            st.t += t0 + t1;
+            float a0, a1, b0, b1;
+            f32x2_unpack(s2, a0, a1);
+            f32x2_unpack(t2, b0, b1);
+            st.s += a0 + a1;
+            st.t += b0 + b1;
             continue;
         }
 #pragma unroll
