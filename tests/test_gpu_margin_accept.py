@@ -135,6 +135,34 @@ def test_full_vocab_planted_ties_across_chunks():
     assert fo[4].cpu().tolist() == [1 + min(i % 7, 6) for i in range(32)]
 
 
+def test_margin_accept_budget_rows_up_to_sixteen():
+    # bf16 rows of requests with up to 16 slots (budget 8N lengths: the finishing warp merges
+    # a request's rows eight at a time), drafts planted to match the row argmax up to a
+    # chosen point: full acceptance of 16, a first-draft miss, and everything in between
+    V, n = 32000, 8
+    g = torch.Generator().manual_seed(21)
+    lengths = [16, 1, 9, 16, 8, 2, 5, 7]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    m_cap = int(cu[-1]) + 3
+    logits = (torch.randn(m_cap, V, generator=g) * 2).to(torch.bfloat16)
+    amax = logits.float().argmax(-1).to(torch.int32)
+    tokens = torch.randint(0, V, (m_cap,), generator=g, dtype=torch.int32)
+    stop = [16, 0, 4, 11, 8, 1, 0, 3]          # drafts that match before the first miss
+    for i in range(n):
+        off, k = int(cu[i]), lengths[i]
+        for j in range(1, k):
+            tokens[off + j] = amax[off + j - 1] if j <= stop[i] else (amax[off + j - 1] + 1) % V
+    outs = svp.margin_accept(logits.cuda(), tokens.cuda(), cu.cuda())
+    torch.cuda.synchronize()
+    live = int(cu[-1])
+    r_idx = _check_rows(logits[:live], [o[:live] for o in outs[:4]])
+    acc, nxt = oracle.greedy_accept(np.concatenate([r_idx, np.zeros(m_cap - live, np.int32)]),
+                                    tokens, cu)
+    assert np.array_equal(outs[4].cpu().numpy(), acc)
+    assert np.array_equal(outs[5].cpu().numpy(), nxt)
+    assert acc.tolist() == [1 + min(stop[i], lengths[i] - 1) for i in range(n)]
+
+
 def test_margin_accept_inactive_and_tail_not_read():
     V = 1000
     g = torch.Generator().manual_seed(3)
