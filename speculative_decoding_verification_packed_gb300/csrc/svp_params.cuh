@@ -35,7 +35,7 @@ struct TcParams {
     float *lse;                  // [m_cap, hq] or nullptr
     int32_t *status;
     int32_t *tickets;            // [n * RB * HG]
-    float *part_o;               // [2 * gridDim.x][128][d]
+    float *part_o;               // verify_tc: [2 * gridDim.x][d / 128][128][128]; attn_tc: [2 * gridDim.x][128][d]
     float2 *part_ml;             // [2 * gridDim.x][128]
     int32_t sig;                 // workspace layout signature (header word 1)
     // transposed short-tile kernel only: tile rows and shared-memory layout

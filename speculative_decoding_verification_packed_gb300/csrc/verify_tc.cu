@@ -316,22 +316,23 @@ __device__ __forceinline__ RingPos ring_add(RingPos r, uint32_t n, uint32_t nslo
     return r;
 }
 
-// One merge pass over NB partial slabs staged in shared memory (ring + q * slab, row-major
-// [nact][D] fp32): acc_r = run_r + sum_q w_q[r] * slab_q[r]; the last pass scales by 1/L and
-// writes bf16 output, earlier ones keep the running sum in the first piece's slot.  Each of the
-// 128 threads owns four columns and takes eight rows at once so that the shared-memory reads of
+// One merge pass over NB partial slabs staged in shared memory: column block h (128 columns
+// of d) of each piece, row-major [nact][128] fp32 at ring + q * slab.  acc_r = run_r +
+// sum_q w_q[r] * slab_q[r]; the last pass of the block scales by 1/L and writes bf16
+// output, earlier ones keep the running sum in the first piece's slot.  Each of the 128
+// threads owns four columns and takes eight rows at once so that the shared-memory reads of
 // all NB x 8 operands are in flight together.
 template <int NB, int D>
 __device__ __forceinline__ void vt_merge_pass(const TcParams &p, const VtRows *rs, uint32_t ring,
                                               uint32_t slab, int32_t wq0, int32_t nact, int32_t slot0,
-                                              bool first_pass, bool last_pass, int stid)
+                                              int h, bool first_pass, bool last_pass, int stid)
 {
-    constexpr int C4 = D / 4;
+    constexpr int C4 = 128 / 4;
     constexpr int RGS = 128 / C4;
     constexpr int RU = 8;
     const int col4 = stid % C4, rg = stid / C4;
-    float4 *run = reinterpret_cast<float4 *>(p.part_o + (int64_t)slot0 * kRows * D) + col4;
-    uint16_t *out = reinterpret_cast<uint16_t *>(p.out) + col4 * 4;
+    float4 *run = reinterpret_cast<float4 *>(p.part_o + ((int64_t)slot0 * (D / 128) + h) * kRows * 128) + col4;
+    uint16_t *out = reinterpret_cast<uint16_t *>(p.out) + h * 128 + col4 * 4;
     const uint32_t col_b = (uint32_t)col4 * 16u;
     for (int r0 = rg; r0 < nact; r0 += RU * RGS) {
         float4 acc[RU];
@@ -347,7 +348,7 @@ __device__ __forceinline__ void vt_merge_pass(const TcParams &p, const VtRows *r
             float w[RU];
 #pragma unroll
             for (int k = 0; k < RU; ++k) {
-                x[k] = ld_shared_f4(ring + q * slab + (uint32_t)rr[k] * (D * 4) + col_b);
+                x[k] = ld_shared_f4(ring + q * slab + (uint32_t)rr[k] * (128 * 4) + col_b);
                 w[k] = rs->wts[wq0 + q][rr[k]];
             }
 #pragma unroll
@@ -1117,7 +1118,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                         for (int e = 0; e < 32; ++e) {
                             const int r = c * 32 + e;
                             if (r < nact)
-                                st_global_f32_hint(p.part_o + ((int64_t)slot * kRows + r) * D + h * 128 + t,
+                                st_global_f32_hint(p.part_o + (((int64_t)slot * DH + h) * kRows + r) * 128 + t,
                                                    __uint_as_float(ro[e]), pol_keep);
                         }
                     }
@@ -1162,20 +1163,22 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 rs->orow[r] = ((int64_t)(out_row0 + r / p.HP) * p.hq + hg * p.HP + r % p.HP) * D;
             }
             named_bar_sync(1, 128);
-            const uint32_t slab = (uint32_t)(((int64_t)nact * D * 4 + 127) / 128 * 128);
+            // a slab is one 128-column block (d-half) of one piece's partial, contiguous in
+            // the [slot][d / 128][row][128] layout; the merge runs block by block
+            const uint32_t slab = (uint32_t)nact * 128u * 4u;
             const int32_t cap_ring = (int32_t)((uint32_t)(nslot * kSlotBytes) / slab);
             const int32_t cap = cap_ring < 8 ? cap_ring : 8;
             // the first pass's slabs are on their way while the row statistics are formed
-            auto issue_pass = [&](int32_t c0) {
+            auto issue_pass = [&](int h, int32_t c0) {
                 const int32_t nb = min(cap, np - c0);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 mbar_arrive_expect_tx(bar_merge, (uint32_t)nb * slab);
                 for (int q = 0; q < nb; ++q)
                     bulk_g2s(sbase + p.off_ring + q * slab,
-                             p.part_o + (int64_t)rs->pslot[c0 + q] * kRows * D, slab, bar_merge);
+                             p.part_o + ((int64_t)rs->pslot[c0 + q] * DH + h) * kRows * 128, slab, bar_merge);
             };
             if (stid == 0)
-                issue_pass(0);
+                issue_pass(0, 0);
             // per row: merged max M and sum L over the pieces, one online pass; with at
             // most 8 pieces the weights 2^(m_q - M) come out of the same pass
             const bool one_block = np <= 8;
@@ -1212,52 +1215,55 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     p.lse[rs->orow[r] / D] = (M + __log2f(Ls)) * 0.69314718055994531f;
             }
             const int32_t slot0 = rs->pslot[0];
-            for (int32_t c0 = 0; c0 < np; c0 += cap) {
-                const int32_t nb = min(cap, np - c0);
-                const int32_t wq0 = one_block ? c0 : 0;   // weights of this pass: wts[wq0 + q]
-                if (c0 > 0) {
-                    if (named_bar_any(1, 128, !ok)) {    // the ring was read by the last pass
-                        ok = false;
-                        break;
+            int32_t npass = 0;
+            for (int h = 0; h < DH && ok; ++h) {
+                for (int32_t c0 = 0; c0 < np; c0 += cap, ++npass) {
+                    const int32_t nb = min(cap, np - c0);
+                    const int32_t wq0 = one_block ? c0 : 0;   // weights of this pass: wts[wq0 + q]
+                    if (npass > 0) {
+                        if (named_bar_any(1, 128, !ok)) {    // the ring was read by the last pass
+                            ok = false;
+                            break;
+                        }
+                        if (stid == 0)
+                            issue_pass(h, c0);
                     }
-                    if (stid == 0)
-                        issue_pass(c0);
-                }
-                if (!one_block && stid < nact) {
-                    const int r = stid;
-                    for (int q = 0; q < nb; ++q)
-                        rs->wts[q][r] = fast_exp2(__ldcg(p.part_ml + (int64_t)rs->pslot[c0 + q] * kRows + r).x -
-                                                  rs->m_ref[r]);
-                }
-                named_bar_sync(1, 128);
-                const bool landed = mbar_wait(bar_merge, merge_phase & 1, abort_flag);
-                if (!landed && stid == 0) {
-                    volatile int drain_abort = 0;   // the slabs land before the CTA exits
-                    mbar_wait(bar_merge, merge_phase & 1, &drain_abort);
-                }
-                ok &= landed;
-                ++merge_phase;
-                const bool last_pass = c0 + cap >= np;
-                const uint32_t ring = sbase + p.off_ring;
-                switch (nb) {
+                    if (!one_block && stid < nact) {
+                        const int r = stid;
+                        for (int q = 0; q < nb; ++q)
+                            rs->wts[q][r] = fast_exp2(__ldcg(p.part_ml + (int64_t)rs->pslot[c0 + q] * kRows + r).x -
+                                                      rs->m_ref[r]);
+                    }
+                    named_bar_sync(1, 128);
+                    const bool landed = mbar_wait(bar_merge, merge_phase & 1, abort_flag);
+                    if (!landed && stid == 0) {
+                        volatile int drain_abort = 0;   // the slabs land before the CTA exits
+                        mbar_wait(bar_merge, merge_phase & 1, &drain_abort);
+                    }
+                    ok &= landed;
+                    ++merge_phase;
+                    const bool last_pass = c0 + cap >= np;
+                    const uint32_t ring = sbase + p.off_ring;
+                    switch (nb) {
 #define SVP_MERGE_CASE(K)                                                                          \
     case K:                                                                                        \
-        vt_merge_pass<K, D>(p, rs, ring, slab, wq0, nact, slot0, c0 == 0, last_pass, stid);        \
+        vt_merge_pass<K, D>(p, rs, ring, slab, wq0, nact, slot0, h, c0 == 0, last_pass, stid);     \
         break;
-                    SVP_MERGE_CASE(1)
-                    SVP_MERGE_CASE(2)
-                    SVP_MERGE_CASE(3)
-                    SVP_MERGE_CASE(4)
-                    SVP_MERGE_CASE(5)
-                    SVP_MERGE_CASE(6)
-                    SVP_MERGE_CASE(7)
-                    default:
-                        vt_merge_pass<8, D>(p, rs, ring, slab, wq0, nact, slot0, c0 == 0, last_pass, stid);
-                        break;
+                        SVP_MERGE_CASE(1)
+                        SVP_MERGE_CASE(2)
+                        SVP_MERGE_CASE(3)
+                        SVP_MERGE_CASE(4)
+                        SVP_MERGE_CASE(5)
+                        SVP_MERGE_CASE(6)
+                        SVP_MERGE_CASE(7)
+                        default:
+                            vt_merge_pass<8, D>(p, rs, ring, slab, wq0, nact, slot0, h, c0 == 0, last_pass, stid);
+                            break;
 #undef SVP_MERGE_CASE
+                    }
+                    if (!last_pass)
+                        __threadfence_block();
                 }
-                if (!last_pass)
-                    __threadfence_block();
             }
             if (named_bar_any(1, 128, !ok)) {
                 ok = false;

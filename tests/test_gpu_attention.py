@@ -288,11 +288,13 @@ def test_workspace_reuse_across_sizes_and_mismatch_flag():
 
 
 @pytest.mark.parametrize("paged", [False, True])
-def test_one_long_pair_split_over_many_ctas(paged):
+@pytest.mark.parametrize("d,hq,k", [(128, 4, 9), (256, 12, 7)])
+def test_one_long_pair_split_over_many_ctas(paged, d, hq, k):
     # a single (request, KV head) pair of ~40 KV tiles is cut into ~40 pieces, so the
-    # last-arrival merge runs several passes of eight pieces
+    # last-arrival merge runs several passes (eight pieces each at d = 128; at d = 256 three
+    # slabs of one 128-column block fit the staging ring, so each block takes many passes)
     b = wl.make_batch("paged_n64_bf16" if paged else "budget8n_bf16", seed=14, n=1,
-                      lengths=[9], ctx_lengths=[5000], hq=4, hkv=1, d=128, poison=True)
+                      lengths=[k], ctx_lengths=[5000], hq=hq, hkv=1, d=d, poison=True)
     out, lse = gpu_verify(to_dev(b))
     ref_o, ref_l = oracle_verify(b)
     compare_attention(out, lse, ref_o, ref_l, rows_of(b), torch.bfloat16)
