@@ -507,6 +507,13 @@ def run_ours(args):
             "rows_per_s": round(fx_rows / (fx_ms / 1e3), 1),
             "kv_gbs": round(kvb / (fx_pl["attn"] / 1e3) / 1e9, 1),
             "short_tile_speedup": round(value / (fx_rows / (fx_ms / 1e3)), 3)}
+        # contrast: the short tile without GQA packing (one query head per tile)
+        un_ms, un_pl, _, _, _ = timed_run(sets, fx_steps, 3, svp, tile_mode=svp.TILE_SHORT_UNPACKED)
+        un_rows = sum(int(sets[s % nsets].cu_slots[-1]) for s in range(fx_steps))
+        extras["unpacked_short_contrast"] = {
+            "rows_per_s": round(un_rows / (un_ms / 1e3), 1),
+            "attn_us": round(un_pl["attn"] * 1e3, 2),
+            "gqa_packing_speedup": round(value / (un_rows / (un_ms / 1e3)), 3)}
         for other in ("budget8n_bf16", "full_width_bf16", "paged_n64_bf16", "wide_gqa_bf16"):
             if other == args.workload:
                 continue
@@ -523,6 +530,8 @@ def run_ours(args):
                  "per_launch_us": {k: round(v * 1e3, 2) for k, v in opl.items()}}
             fms, fpl, _, _, _ = timed_run(osets, st, 3, svp, tile_mode=svp.TILE_FIXED128)
             e["fixed128_rows_per_s"] = round(orows / (fms / 1e3), 1)
+            ums, upl, _, _, _ = timed_run(osets, st, 3, svp, tile_mode=svp.TILE_SHORT_UNPACKED)
+            e["unpacked_short_rows_per_s"] = round(orows / (ums / 1e3), 1)
             if "draft_margin" in opl:
                 V = osets[0].target_logits.shape[1]
                 e["draft_margin_gbs"] = round(osets[0].draft_logits.numel() * 2 /

@@ -76,7 +76,11 @@ typedef enum {
                                are packed into one tile of G*min(w, 128/G) rows; split-KV   */
     SVP_TILE_FIXED128 = 2,  /* contrast: one query head per 128-row tile, one block per
                                (request, head), no split (the prior-art native tile)       */
-    SVP_TILE_WIDE = 3       /* prefill-style 128-row tile of one head, split-KV            */
+    SVP_TILE_WIDE = 3,      /* prefill-style 128-row tile of one head, split-KV            */
+    SVP_TILE_SHORT_UNPACKED = 4  /* contrast: the candidate-width tile without GQA packing:
+                               one query head per tile of min(w, 128) rows (96 at d = 256),
+                               so each KV head is streamed once per query head; split-KV;
+                               d = 128 or 256                                              */
 } svp_tile_mode;
 
 /* GQA head layout.  Query head h reads KV head h / (hq / hkv). */

@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libsvp.so")
 
 SVP_OK, SVP_EINVAL, SVP_EUNSUPPORTED, SVP_EWORKSPACE, SVP_ECUDA = 0, 1, 2, 3, 4
 SVP_F32, SVP_BF16 = 0, 1
-TILE_AUTO, TILE_SHORT, TILE_FIXED128, TILE_WIDE = 0, 1, 2, 3
+TILE_AUTO, TILE_SHORT, TILE_FIXED128, TILE_WIDE, TILE_SHORT_UNPACKED = 0, 1, 2, 3, 4
 DEV_BAD_SLOTS, DEV_BAD_CONTEXT, DEV_TIMEOUT, DEV_WORKSPACE = 0x1, 0x2, 0x4, 0x8
 
 

@@ -132,6 +132,21 @@ static svp_status attn_plan(int32_t n, int32_t w, int32_t hq, int32_t hkv, int32
         pl.split = 1;
         break;
     }
+    case SVP_TILE_SHORT_UNPACKED: {
+        // contrast: the same transposed kernel with one query head per tile, so every query
+        // head streams its KV head itself (G times the KV bytes of the packed tile)
+        if (d == 64)
+            return SVP_EUNSUPPORTED;
+        const int nr_cap = (d == 256) ? 96 : 128;
+        pl.transposed = 1;
+        pl.HP = 1;
+        pl.R = std::min(w, nr_cap);
+        pl.NR = (pl.R + 31) / 32 * 32;
+        pl.HG = hq;
+        pl.CB = 16;
+        pl.split = 1;
+        break;
+    }
     case SVP_TILE_FIXED128:
         pl.HP = 1;
         pl.R = std::min(w, 128);

@@ -127,11 +127,22 @@ def test_packed_equals_alone_and_relayout_on_gpu():
     assert d <= 1e-2
 
 
-@pytest.mark.parametrize("mode", [svp.TILE_FIXED128, svp.TILE_SHORT, svp.TILE_WIDE])
+@pytest.mark.parametrize("mode", [svp.TILE_FIXED128, svp.TILE_SHORT, svp.TILE_WIDE,
+                                  svp.TILE_SHORT_UNPACKED])
 def test_tile_modes_match_oracle(mode):
     b = wl.make_batch("budget8n_bf16", seed=5, n=4, lengths=[16, 2, 11, 5],
                       ctx_lengths=[513, 64, 1500, 0], hq=8, hkv=2, d=128, poison=True)
     out, lse = gpu_verify(to_dev(b), tile_mode=mode)
+    ref_o, ref_l = oracle_verify(b)
+    compare_attention(out, lse, ref_o, ref_l, rows_of(b), torch.bfloat16)
+
+
+def test_unpacked_short_tile_at_head_dim_256():
+    # the GQA-unpacked contrast at d = 256 (one query head per 32-row tile, 12 heads per KV
+    # head), with split pairs and contexts ending mid-tile
+    b = wl.make_batch("wide_gqa_bf16", seed=8, n=3, lengths=[7, 3, 7], ctx_lengths=[700, 130, 0],
+                      hq=12, hkv=1, d=256, poison=True, with_logits=False)
+    out, lse = gpu_verify(to_dev(b), tile_mode=svp.TILE_SHORT_UNPACKED)
     ref_o, ref_l = oracle_verify(b)
     compare_attention(out, lse, ref_o, ref_l, rows_of(b), torch.bfloat16)
 
