@@ -90,3 +90,21 @@ def compare_attention(out_gpu, lse_gpu, ref_o, ref_l, rows, dtype):
             assert stats["lse_max_abs"] <= BF16_LSE_ABS, stats
     assert np.isfinite(o).all()
     return stats
+
+
+def _bits(a):
+    return np.asarray(a, dtype=np.float32).view(np.int32)
+
+
+def check_margin_rows(logits_cpu, outs, rows=None):
+    """Row top-1 index, top-1, top-2 and margin bit for bit against the oracle's scalar
+    scan (NaN margins must match as NaN); returns the oracle's argmax indices."""
+    idx, t1, t2, mg = (o.cpu().numpy() for o in outs[:4])
+    r_idx, r_t1, r_t2, r_mg = oracle.row_top2(logits_cpu)
+    sel = slice(None) if rows is None else rows
+    assert np.array_equal(idx[sel], r_idx[sel])
+    assert np.array_equal(_bits(t1[sel]), _bits(r_t1[sel]))
+    assert np.array_equal(_bits(t2[sel]), _bits(r_t2[sel]))
+    ok = (_bits(mg[sel]) == _bits(r_mg[sel])) | (np.isnan(mg[sel]) & np.isnan(r_mg[sel]))
+    assert ok.all()
+    return r_idx

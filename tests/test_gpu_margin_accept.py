@@ -10,24 +10,12 @@ import torch
 import oracle
 import speculative_decoding_verification_packed_gb300 as svp
 from speculative_decoding_verification_packed_gb300 import workloads as wl
+from helpers import check_margin_rows
 
 pytestmark = pytest.mark.gpu
 
 
-def _bits(a):
-    return np.asarray(a, dtype=np.float32).view(np.int32)
-
-
-def _check_rows(logits_cpu, outs, rows=None):
-    idx, t1, t2, mg = (o.cpu().numpy() for o in outs[:4])
-    r_idx, r_t1, r_t2, r_mg = oracle.row_top2(logits_cpu)
-    sel = slice(None) if rows is None else rows
-    assert np.array_equal(idx[sel], r_idx[sel])
-    assert np.array_equal(_bits(t1[sel]), _bits(r_t1[sel]))
-    assert np.array_equal(_bits(t2[sel]), _bits(r_t2[sel]))
-    ok = (_bits(mg[sel]) == _bits(r_mg[sel])) | (np.isnan(mg[sel]) & np.isnan(r_mg[sel]))
-    assert ok.all()
-    return r_idx
+_check_rows = check_margin_rows
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
