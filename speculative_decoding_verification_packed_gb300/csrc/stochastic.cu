@@ -388,21 +388,30 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
                         (reinterpret_cast<uintptr_t>(p.logits) & 15) == 0;
     float own = 0.0f;
     int64_t e = lo;
+    uint4 xb[8];   // the last batch of vectors; with at most eight it is the thread's whole run
     if (vec_ok) {
         const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.logits) +
                                                            (rowb + lo) * (DT == 1 ? 2 : 4));
         const int64_t nv = hi > lo ? (hi - lo) / VEC : 0;
-        for (int64_t v = 0; v < nv; ++v) {
-            const uint4 x = __ldg(src + v);
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        for (int64_t v0 = 0; v0 < nv; v0 += 8) {   // eight vectors in flight, summed in order
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                if (DT == 1) {
-                    const int64_t e2 = lo + v * VEC + 2 * h;
-                    own += e2 != excl ? exp2f((bf16_lo(w[h]) - m) * p.c) : 0.0f;
-                    own += e2 + 1 != excl ? exp2f((bf16_hi(w[h]) - m) * p.c) : 0.0f;
-                } else {
-                    own += lo + v * VEC + h != excl ? exp2f((__uint_as_float(w[h]) - m) * p.c) : 0.0f;
+            for (int q = 0; q < 8; ++q)
+                xb[q] = v0 + q < nv ? __ldg(src + v0 + q) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (v0 + q >= nv)
+                    break;
+                const int64_t v = v0 + q;
+                const uint32_t w[4] = {xb[q].x, xb[q].y, xb[q].z, xb[q].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    if (DT == 1) {
+                        const int64_t e2 = lo + v * VEC + 2 * h;
+                        own += e2 != excl ? exp2f((bf16_lo(w[h]) - m) * p.c) : 0.0f;
+                        own += e2 + 1 != excl ? exp2f((bf16_hi(w[h]) - m) * p.c) : 0.0f;
+                    } else {
+                        own += lo + v * VEC + h != excl ? exp2f((__uint_as_float(w[h]) - m) * p.c) : 0.0f;
+                    }
                 }
             }
         }
@@ -446,20 +455,53 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
     // with weight
     const int who = claim < kStThreads2 ? claim : sh_lastnz;
     if (tid == who) {
+        // the same weights in the same order as the sum above; the thread's 16-byte vectors
+        // come eight at a time (one round trip per batch, none when the run fits one batch)
         float cum = before;
         int32_t y = -1, lnz = -1;
-        for (int64_t e = lo; e < hi; ++e) {
-            if (e == excl)
-                continue;
-            const float w = exp2f((st_load<DT>(p.logits, rowb + e) - m) * p.c);
+        bool found = false;
+        const bool want = claim < kStThreads2;
+        auto take = [&](int64_t e2, float v) {
+            if (found || e2 == excl)
+                return;
+            const float w = exp2f((v - m) * p.c);
             if (w > 0.0f)
-                lnz = (int32_t)e;
+                lnz = (int32_t)e2;
             cum += w;
-            if (claim < kStThreads2 && cum > target && w > 0.0f) {
-                y = (int32_t)e;
-                break;
+            if (want && cum > target && w > 0.0f) {
+                y = (int32_t)e2;
+                found = true;
             }
+        };
+        int64_t e3 = lo;
+        if (vec_ok) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.logits) +
+                                                               (rowb + lo) * (DT == 1 ? 2 : 4));
+            const int64_t nv = hi > lo ? (hi - lo) / VEC : 0;
+            for (int64_t v0 = 0; v0 < nv && !found; v0 += 8) {
+                if (nv > 8) {   // otherwise the vectors summed above are still in xb
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        xb[q] = v0 + q < nv ? __ldg(src + v0 + q) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                for (int q = 0; q < 8 && v0 + q < nv && !found; ++q) {
+                    const uint32_t w4[4] = {xb[q].x, xb[q].y, xb[q].z, xb[q].w};
+                    const int64_t eb = lo + (v0 + q) * VEC;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (DT == 1) {
+                            take(eb + 2 * h, bf16_lo(w4[h]));
+                            take(eb + 2 * h + 1, bf16_hi(w4[h]));
+                        } else {
+                            take(eb + h, __uint_as_float(w4[h]));
+                        }
+                    }
+                }
+            }
+            e3 = lo + nv * VEC;
         }
+        for (; e3 < hi && !found; ++e3)
+            take(e3, st_load<DT>(p.logits, rowb + e3));
         p.next_token[i] = y >= 0 ? y : lnz;
     }
     if (tid == 0 && who < 0)
