@@ -171,9 +171,14 @@ svp_status svp_prefill_attn_workspace_size(int32_t n, int32_t max_s,
 /*
  * q [total_s, hq, d], k, v [total_s, hkv, d]  sequences packed by cu_seqlens
  * cu_seqlens [n+1] int32 (device)  row offsets; sequence lengths <= max_s (host bound)
- * causal   must be 1
+ * causal   must be 1 (SVP_EUNSUPPORTED otherwise)
  * out [total_s, hq, d] (dtype), lse [total_s, hq] fp32 (may be NULL)
- * SVP_BF16 only.
+ * SVP_BF16 only; 0 <= total_s < 2^31 (SVP_EINVAL otherwise).
+ * Routing: d = 128 with an even number of query heads per KV head, 1 <= n <= 16 and
+ *   max_s <= 32768 run the dedicated kernel (q, k, v, out 16-byte aligned, else
+ *   SVP_EINVAL; it uses only the workspace header); every other shape runs the general
+ *   128-row attention kernel.  A sequence whose offsets run backwards, leave the buffer or
+ *   exceed max_s is skipped and sets SVP_DEV_BAD_SLOTS in the workspace status word.
  */
 svp_status svp_prefill_attn(const void *q, const void *k, const void *v,
                             const int32_t *cu_seqlens, int32_t n, int32_t max_s,
