@@ -282,12 +282,105 @@ __device__ __forceinline__ void ft_top4(uint32_t &t0, uint32_t &t1, uint32_t &t2
     t2 = bf16x2_max(t2, y2);
 }
 
+// Compare-exchange of packed pairs: a takes the larger, b the smaller value of each half.
+__device__ __forceinline__ void ft_cx(uint32_t &a, uint32_t &b)
+{
+    const uint32_t h = bf16x2_max(a, b);
+    b = bf16x2_min(a, b);
+    a = h;
+}
+
+// Per-stream top 4 after one batch of 8 new packed pairs v[0..7] (one per vector): the
+// pairs are sorted, merged into two sorted quadruples (odd-even merge), the top 4 of both
+// taken as a bitonic half and sorted; that list is merged into (t0 >= t1 >= t2 >= t3) the
+// same way.  44 packed min / max against 56 for eight single insertions.  Returns the
+// batch maximum of each half.
+__device__ __forceinline__ uint32_t ft_top4_batch(uint32_t &t0, uint32_t &t1, uint32_t &t2,
+                                                  uint32_t &t3, uint32_t (&v)[8])
+{
+    ft_cx(v[0], v[1]);
+    ft_cx(v[2], v[3]);
+    ft_cx(v[4], v[5]);
+    ft_cx(v[6], v[7]);
+    ft_cx(v[0], v[2]);
+    ft_cx(v[1], v[3]);
+    ft_cx(v[1], v[2]);
+    ft_cx(v[4], v[6]);
+    ft_cx(v[5], v[7]);
+    ft_cx(v[5], v[6]);
+    uint32_t c0 = bf16x2_max(v[0], v[7]), c1 = bf16x2_max(v[1], v[6]);
+    uint32_t c2 = bf16x2_max(v[2], v[5]), c3 = bf16x2_max(v[3], v[4]);
+    ft_cx(c0, c2);
+    ft_cx(c1, c3);
+    ft_cx(c0, c1);
+    ft_cx(c2, c3);
+    uint32_t u0 = bf16x2_max(t0, c3), u1 = bf16x2_max(t1, c2);
+    uint32_t u2 = bf16x2_max(t2, c1), u3 = bf16x2_max(t3, c0);
+    ft_cx(u0, u2);
+    ft_cx(u1, u3);
+    ft_cx(u0, u1);
+    ft_cx(u2, u3);
+    t0 = u0;
+    t1 = u1;
+    t2 = u2;
+    t3 = u3;
+    return c0;
+}
+
+// Sums (s, t) of one lane's batch against the reference ml = m log2 e: both values of a
+// packed pair at once (d = z log2 e - ml by one packed fma, the sum and the weighted sum by
+// one packed add and one packed fma).  CLAMP reads -inf as -9.97e37 (weight 0, finite d);
+// without it a -inf value makes t NaN (0 * -inf).
+template <bool CLAMP>
+__device__ __forceinline__ void ft_batch_sums(const uint4 (&x)[kFtLoads], float ml, float &s,
+                                              float &t)
+{
+    const uint64_t l2e2 = f32x2_pack(kFtL2e, kFtL2e), nml2 = f32x2_pack(-ml, -ml);
+    uint64_t s2 = f32x2_pack(0.0f, 0.0f), t2 = s2;
+#pragma unroll
+    for (int q = 0; q < kFtLoads; ++q) {
+        const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t c = CLAMP ? bf16x2_max(w[k], kFtLow2) : w[k];
+            const uint64_t d2 = f32x2_fma(f32x2_pack(bf16_lo(c), bf16_hi(c)), l2e2, nml2);
+            float d0, d1;
+            f32x2_unpack(d2, d0, d1);
+            const uint64_t e2 = f32x2_pack(fast_exp2(d0), fast_exp2(d1));
+            s2 = f32x2_add(s2, e2);
+            t2 = f32x2_fma(e2, d2, t2);
+        }
+    }
+    float a0, a1, b0, b1;
+    f32x2_unpack(s2, a0, a1);
+    f32x2_unpack(t2, b0, b1);
+    s = a0 + a1;
+    t = b0 + b1;
+}
+
+// Order-preserving codes of both bf16 halves of w (unsigned order of the codes = order of
+// the values; -0 sits just below +0): a set sign bit flips all 16 bits, a clear one only
+// the sign bit.
+__device__ __forceinline__ uint32_t ft_ord2(uint32_t w)
+{
+    const uint32_t sg = (w >> 15) & 0x00010001u;
+    return w ^ (sg * 0x7fffu + 0x80008000u);
+}
+
+// The value of a draw key (its code in the high half).
+__device__ __forceinline__ float ft_unord(uint32_t key)
+{
+    const uint32_t o = key >> 16;
+    return __uint_as_float((o ^ ((o & 0x8000u) ? 0x8000u : 0xffffu)) << 16);
+}
+
+__device__ __forceinline__ uint32_t ft_max8(const uint32_t (&k)[8])
+{
+    return max(max(max(k[0], k[1]), max(k[2], k[3])), max(max(k[4], k[5]), max(k[6], k[7])));
+}
+
 __device__ __forceinline__ float ft_hmax(uint32_t w) { return fmaxf(bf16_lo(w), bf16_hi(w)); }
 
-__device__ __forceinline__ float ft_hmax4(const uint32_t (&t)[4])
-{
-    return ft_hmax(bf16x2_max(bf16x2_max(t[0], t[1]), bf16x2_max(t[2], t[3])));
-}
 
 // bf16 rows with 16-byte alignment.  Every lane has 8 streams (packed word k of its vectors,
 // low or high half); each stream keeps its top 4 with packed bf16 min / max, branch-free.
@@ -313,62 +406,38 @@ __device__ __forceinline__ bool ft_scan_bf16(const FtParams &p, int64_t rowb, in
             const int64_t v = v0 + q * 32 + lane;
             x[q] = v < nv ? __ldg(src + v) : make_uint4(kFtNegInf2, kFtNegInf2, kFtNegInf2, kFtNegInf2);
         }
-        if (v0 + kFtLoads * 32 <= nv) {
-            // a full batch (warp-uniform): the top-4 updates and the batch maximum, one
-            // rebase, then the statistics of all 64 values in two chains
+        // the statistics of the lane's 64 values against the running reference st.m (the
+        // first batch of a chunk takes its reference from the lane's first vector), then the
+        // top-4 network of each word in place, whose batch maximum moves the reference
+        if (st.m == -INFINITY)
+            st.m = ft_hmax(bf16x2_max(bf16x2_max(bf16x2_max(x[0].x, x[0].y), bf16x2_max(x[0].z, x[0].w)),
+                                      kFtLow2));
+        float bs, bt;
+        const bool full = v0 + kFtLoads * 32 <= nv;   // warp-uniform; a partial batch holds -inf
+        if (full)
+            ft_batch_sums<false>(x, st.m * kFtL2e, bs, bt);
+        if (!full || !(bs <= 1e37f && fabsf(bt) <= 1e37f)) {
+            // a -inf value (t is NaN) or values far above the reference: move the reference
+            // to the batch maximum first and read -inf as -9.97e37
             uint32_t b2 = kFtLow2;
 #pragma unroll
-            for (int q = 0; q < kFtLoads; ++q) {
-                const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    ft_top4(T0[k], T1[k], T2[k], T3[k], w[k]);
-                    b2 = bf16x2_max(b2, w[k]);
-                }
-            }
+            for (int q = 0; q < kFtLoads; ++q)
+                b2 = bf16x2_max(b2, bf16x2_max(bf16x2_max(x[q].x, x[q].y), bf16x2_max(x[q].z, x[q].w)));
             ft_stat_rebase(st, ft_hmax(b2));
-            const float ml = st.m * kFtL2e;
-            // both values of a packed pair at once: d = z log2 e - m log2 e by one packed fma,
-            // the sum and the weighted sum by one packed add and one packed fma
-            const uint64_t l2e2 = f32x2_pack(kFtL2e, kFtL2e), nml2 = f32x2_pack(-ml, -ml);
-            uint64_t s2 = f32x2_pack(0.0f, 0.0f), t2 = s2;
-#pragma unroll
-            for (int q = 0; q < kFtLoads; ++q) {
-                const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t c = bf16x2_max(w[k], kFtLow2);
-                    const uint64_t d2 = f32x2_fma(f32x2_pack(bf16_lo(c), bf16_hi(c)), l2e2, nml2);
-                    float d0, d1;
-                    f32x2_unpack(d2, d0, d1);
-                    const uint64_t e2 = f32x2_pack(fast_exp2(d0), fast_exp2(d1));
-                    s2 = f32x2_add(s2, e2);
-                    t2 = f32x2_fma(e2, d2, t2);
-                }
-            }
-            float a0, a1, b0, b1;
-            f32x2_unpack(s2, a0, a1);
-            f32x2_unpack(t2, b0, b1);
-            st.s += a0 + a1;
-            st.t += b0 + b1;
-            continue;
+            ft_batch_sums<true>(x, st.m * kFtL2e, bs, bt);
         }
+        st.s += bs;
+        st.t += bt;
+        uint32_t b2 = kFtLow2;
 #pragma unroll
-        for (int q = 0; q < kFtLoads; ++q) {
-            if (v0 + q * 32 + lane >= nv)
-                continue;
-            const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-            uint32_t c[4];
-            float f[8];
+        for (int k = 0; k < 4; ++k) {
+            uint32_t v[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                ft_top4(T0[k], T1[k], T2[k], T3[k], w[k]);
-                c[k] = bf16x2_max(w[k], kFtLow2);
-                f[2 * k] = bf16_lo(c[k]);
-                f[2 * k + 1] = bf16_hi(c[k]);
-            }
-            ft_stat_acc<8, false>(st, f, ft_hmax4(c));
+            for (int q = 0; q < kFtLoads; ++q)
+                v[q] = k == 0 ? x[q].x : k == 1 ? x[q].y : k == 2 ? x[q].z : x[q].w;
+            b2 = bf16x2_max(b2, ft_top4_batch(T0[k], T1[k], T2[k], T3[k], v));
         }
+        ft_stat_rebase(st, ft_hmax(b2));
     }
     for (int64_t e = lo + nv * 8 + lane; e < hi; e += 32) {   // fewer than 8 values
         const uint32_t b = __ldg(reinterpret_cast<const uint16_t *>(p.logits) + rowb + e);
@@ -378,41 +447,51 @@ __device__ __forceinline__ bool ft_scan_bf16(const FtParams &p, int64_t rowb, in
         f[0] = bf16_lo(bf16x2_max(w, kFtLow2));
         ft_stat_acc<1, false>(st, f, f[0]);
     }
-    const float fourth = ft_hmax4(T3);   // before any entry is drawn
-    float v16 = -INFINITY;
+    // the draw, on 32-bit keys: the order-preserving code of the value in the high half,
+    // then (31 - lane, 7 - stream) so that every entry's key is unique; K0[j] is the key of
+    // stream j's head (stream j = half j & 1 of word j >> 1)
+    uint32_t K0[8], K1[8], K2[8], K3[8];
+    const uint32_t ltag = (uint32_t)(31 - lane) << 3;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t tlo = ltag | (uint32_t)(7 - 2 * k), thi = ltag | (uint32_t)(6 - 2 * k);
+        const uint32_t o0 = ft_ord2(T0[k]), o1 = ft_ord2(T1[k]), o2 = ft_ord2(T2[k]), o3 = ft_ord2(T3[k]);
+        K0[2 * k] = (o0 << 16) | tlo;
+        K0[2 * k + 1] = (o0 & 0xffff0000u) | thi;
+        K1[2 * k] = (o1 << 16) | tlo;
+        K1[2 * k + 1] = (o1 & 0xffff0000u) | thi;
+        K2[2 * k] = (o2 << 16) | tlo;
+        K2[2 * k + 1] = (o2 & 0xffff0000u) | thi;
+        K3[2 * k] = (o3 << 16) | tlo;
+        K3[2 * k + 1] = (o3 & 0xffff0000u) | thi;
+    }
+    const uint32_t fourth = ft_max8(K3);   // before any entry is drawn
+    uint32_t head = ft_max8(K0), kmax = 0, slot = 0;
 #pragma unroll 1
     for (int rnd = 0; rnd < kFtTop; ++rnd) {
-        const float head = ft_hmax4(T0);
-        float best = head;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+        kmax = __reduce_max_sync(0xffffffffu, head);
         if (lane == rnd)
-            top.slot = best;
-        v16 = best;
-        const uint32_t win = __ballot_sync(0xffffffffu, head == best);
-        if (lane == __ffs(win) - 1) {
-            // the first of this lane's streams whose head is `best` moves up one entry
-            bool done = false;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const uint32_t hm = hf ? 0xffff0000u : 0x0000ffffu;
-                    const float hv = hf ? bf16_hi(T0[k]) : bf16_lo(T0[k]);
-                    if (!done && hv == best) {
-                        T0[k] = (T0[k] & ~hm) | (T1[k] & hm);
-                        T1[k] = (T1[k] & ~hm) | (T2[k] & hm);
-                        T2[k] = (T2[k] & ~hm) | (T3[k] & hm);
-                        T3[k] = (T3[k] & ~hm) | (kFtNegInf2 & hm);
-                        done = true;
-                    }
-                }
+            slot = kmax;
+        if (head == kmax) {   // the one lane holding the drawn entry: its stream moves up
+            switch (7 - (int)(kmax & 7u)) {
+#define FT_POP(J)                                                                          \
+    case J:                                                                                \
+        K0[J] = K1[J];                                                                     \
+        K1[J] = K2[J];                                                                     \
+        K2[J] = K3[J];                                                                     \
+        K3[J] = 0u;                                                                        \
+        break;
+                FT_POP(0) FT_POP(1) FT_POP(2) FT_POP(3) FT_POP(4) FT_POP(5) FT_POP(6) FT_POP(7)
+#undef FT_POP
             }
+            head = ft_max8(K0);
         }
     }
-    top.tau = v16;
-    return __ballot_sync(0xffffffffu, fourth >= v16) == 0;
+    if (lane < kFtTop)
+        top.slot = ft_unord(slot);
+    top.tau = ft_unord(kmax);
+    // exact unless a stream's fourth entry reaches the 16th drawn value
+    return __ballot_sync(0xffffffffu, (fourth >> 16) >= (kmax >> 16)) == 0;
 }
 
 // Top-16 of a row from its chunks' sorted top-16 lists (kFtPart floats apart): lane l holds
@@ -450,7 +529,7 @@ __device__ __forceinline__ void ft_merge_lists(const float *lists, int32_t nl, i
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kFtThreads) features_kernel(const FtParams p)
+__global__ void __launch_bounds__(kFtThreads, 3) features_kernel(const FtParams p)
 {
     const int lane = threadIdx.x & 31;
     const int64_t warp_g = ((int64_t)blockIdx.x * kFtThreads + threadIdx.x) >> 5;

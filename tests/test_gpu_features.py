@@ -97,3 +97,18 @@ def test_full_size_wide_gqa_sampled_rows():
     assert np.abs(o[:, 16] - ref[:, 16]).max() <= 1e-4
     assert np.abs(o[:, 17] - ref[:, 17]).max() <= 1e-4 * np.log(V)
     assert np.all(np.isfinite(out))
+
+
+@pytest.mark.parametrize("rows,V,pad", [(4000, 1000, 0), (4500, 2999, 1)])
+def test_features_several_units_per_warp(rows, V, pad):
+    """More rows than resident warps: warps take several (row, chunk) units in turn, each
+    chunk ending in a partial batch (and, for V = 2999, a tail of fewer than 8 values)."""
+    g = torch.Generator().manual_seed(rows)
+    z = (torch.randn(rows, V + pad, generator=g) * 3.0).to(torch.bfloat16)
+    ref = ft.draft_features(z.float().numpy()[:, :V].astype(np.float64))
+    ws = svp.Workspace(svp.draft_features_workspace_size(rows, V))
+    out = svp.draft_features(z.cuda(), vocab=V, ws=ws).cpu().numpy().astype(np.float64)
+    assert out[:, 0].tolist() == ref[:, 0].tolist()
+    assert np.all(np.abs(out[:, 1:16] - ref[:, 1:16]) <= 6e-8 * np.maximum(np.abs(ref[:, 1:16]), np.abs(ref[:, :1])))
+    assert np.abs(out[:, 16] - ref[:, 16]).max() <= 1e-4
+    assert np.abs(out[:, 17] - ref[:, 17]).max() <= 1e-4 * np.log(V)
