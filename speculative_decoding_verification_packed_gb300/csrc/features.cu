@@ -162,15 +162,41 @@ __device__ __forceinline__ void ft_stat_merge(FtStat &st, float m2, float s2, fl
     st.m = M;
 }
 
+// Order-preserving 32-bit code of a float (unsigned order of the codes = order of the
+// values, -0 just below +0; no NaN) and its inverse.
+__device__ __forceinline__ uint32_t ft_ord32(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ float ft_unord32(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// Fold the 32 lanes' (m, s, t): the warp maximum M by one redux, each lane's sums moved to
+// M, then a butterfly sum.  Every lane ends with the warp's (M, s, t).
 __device__ __forceinline__ void ft_stat_warp(FtStat &st)
 {
+    const float M = ft_unord32(__reduce_max_sync(0xffffffffu, ft_ord32(st.m)));
+    if (M == -INFINITY)   // warp-uniform: no lane saw a value
+        return;
+    float s = 0.0f, t = 0.0f;
+    if (st.m != -INFINITY) {
+        const float d = (st.m - M) * kFtL2e;
+        const float a = exp2f(d);
+        s = a * st.s;
+        t = a > 0.0f ? a * (st.t + st.s * d) : 0.0f;   // d may be huge: no 0 * inf
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, st.s, o);
-        const float t2 = __shfl_xor_sync(0xffffffffu, st.t, o);
-        ft_stat_merge(st, m2, s2, t2);
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+        t += __shfl_xor_sync(0xffffffffu, t, o);
     }
+    st.m = M;
+    st.s = s;
+    st.t = t;
 }
 
 // Lane 0 writes the 18 features of row r (top values gathered from lanes 0..15).
@@ -495,8 +521,9 @@ __device__ __forceinline__ bool ft_scan_bf16(const FtParams &p, int64_t rowb, in
 }
 
 // Top-16 of a row from its chunks' sorted top-16 lists (kFtPart floats apart): lane l holds
-// list l of a batch of 31 (lane 31 the top-16 so far), and 16 rounds of warp maximum draw
-// the next batch top-16 (the lowest lane holding the maximum gives up its head).
+// list l of a batch of 31 (lane 31 the top-16 so far), and 16 rounds of warp maximum (one
+// redux on the heads' order codes) draw the next batch top-16; the lowest lane holding the
+// maximum gives up its head.
 __device__ __forceinline__ void ft_merge_lists(const float *lists, int32_t nl, int lane, FtTop &top)
 {
     for (int32_t b0 = 0; b0 < nl; b0 += 31) {
@@ -507,16 +534,14 @@ __device__ __forceinline__ void ft_merge_lists(const float *lists, int32_t nl, i
             const float run = __shfl_sync(0xffffffffu, top.slot, k);
             l[k] = lane == 31 ? run : (lane < 31 && q < nl ? __ldcg(lists + (int64_t)q * kFtPart + k) : -INFINITY);
         }
-        float best = -INFINITY;
+        uint32_t kmax = 0;
 #pragma unroll 1
         for (int rnd = 0; rnd < kFtTop; ++rnd) {
-            best = l[0];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+            const uint32_t key = ft_ord32(l[0]);
+            kmax = __reduce_max_sync(0xffffffffu, key);
             if (lane == rnd)
-                top.slot = best;
-            const uint32_t win = __ballot_sync(0xffffffffu, l[0] == best);
+                top.slot = ft_unord32(kmax);
+            const uint32_t win = __ballot_sync(0xffffffffu, key == kmax);
             if (lane == __ffs(win) - 1) {
 #pragma unroll
                 for (int k = 0; k < kFtTop - 1; ++k)
@@ -524,7 +549,7 @@ __device__ __forceinline__ void ft_merge_lists(const float *lists, int32_t nl, i
                 l[kFtTop - 1] = -INFINITY;
             }
         }
-        top.tau = best;
+        top.tau = ft_unord32(kmax);
     }
 }
 
@@ -574,14 +599,13 @@ __global__ void __launch_bounds__(kFtThreads, 3) features_kernel(const FtParams 
                 pp[17] = st.s;
                 pp[18] = st.t;
             }
-            __threadfence();   // every lane's partial stores before the ticket
-            __syncwarp();
+            __syncwarp();   // every lane's partial stores before lane 0's release
             if (lane == 0)
-                last = atomicAdd(p.tickets + r, 1) == p.chunks - 1;
+                last = ticket_add_acq_rel(p.tickets + r, 1) == p.chunks - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
-            __threadfence();
+            __syncwarp();   // lane 0's acquire orders the other lanes' reads
             FtTop mg;
             ft_top_init(mg);
             ft_merge_lists(p.partial + (int64_t)r * p.chunks * kFtPart, p.chunks, lane, mg);
