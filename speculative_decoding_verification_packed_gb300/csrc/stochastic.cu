@@ -112,6 +112,9 @@ __device__ __forceinline__ void st_acc(float &m, float &mc, float &s, const floa
 template <int DT>
 __global__ void __launch_bounds__(kStThreads1, 4) st_rowstat_kernel(const StParams p)
 {
+    // the grid always fits in one wave (at most 4 CTAs per SM): the acceptance pass may be
+    // scheduled as soon as every CTA has started, onto SMs as this pass frees them
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warp_g = ((int64_t)blockIdx.x * kStThreads1 + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kStThreads1) >> 5;
@@ -236,9 +239,22 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
     __shared__ int32_t sh_row, sh_excl, sh_chunk, sh_claim, sh_lastnz;
     const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t off = __ldg(p.cu_slots + i), end = __ldg(p.cu_slots + i + 1);
+    const bool meta_ok = off >= 0 && end >= off && end <= p.m_cap;
+    // before the wait for the statistics pass: what depends on the inputs only.  Warp 0
+    // brings the first 32 candidates' tokens, their logits on the rows they are tested on
+    // and their acceptance draws.
+    int32_t x_pre = -1;
+    float z_pre = -INFINITY, u_pre = 0.0f;
+    if (warp == 0 && meta_ok && 1 + lane < end - off) {
+        const int32_t j = 1 + lane;
+        x_pre = __ldg(p.tokens + off + j);
+        if (x_pre >= 0 && x_pre < p.vocab)
+            z_pre = st_load<DT>(p.logits, (int64_t)(off + j - 1) * p.row_stride + x_pre);
+        u_pre = __ldg(p.u_accept + off + j);
+    }
+    griddep_wait();
     // the first pass found cu_slots invalid (it set the status bit): nothing was read
-    if (*reinterpret_cast<volatile int32_t *>(p.status + 2) != 0 || off < 0 || end < off ||
-        end > p.m_cap) {
+    if (*reinterpret_cast<volatile int32_t *>(p.status + 2) != 0 || !meta_ok) {
         if (tid == 0) {
             p.accept_len[i] = 0;
             p.next_token[i] = -1;
@@ -277,14 +293,22 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
             bool pass = true;
             if (j < k) {
                 const int32_t r = off + j - 1;
-                x = __ldg(p.tokens + off + j);
+                float u;
+                if (j0 == 1) {   // brought before the wait
+                    x = x_pre;
+                    z = z_pre;
+                    u = u_pre;
+                } else {
+                    x = __ldg(p.tokens + off + j);
+                    if (x >= 0 && x < p.vocab)
+                        z = st_load<DT>(p.logits, (int64_t)r * p.row_stride + x);
+                    u = __ldg(p.u_accept + off + j);
+                }
                 const float2 st = __ldcg(p.row_stat + r);
                 mr = st.x;
-                if (x >= 0 && x < p.vocab) {
-                    z = st_load<DT>(p.logits, (int64_t)r * p.row_stride + x);
+                if (x >= 0 && x < p.vocab)
                     pr = exp2f((z - st.x) * p.c) / st.y;
-                }
-                pass = __ldg(p.u_accept + off + j) < pr;
+                pass = u < pr;
             }
             const uint32_t rej = __ballot_sync(0xffffffffu, !pass);
             const int first = rej ? __ffs(rej) - 1 : 32;
@@ -599,12 +623,29 @@ extern "C" svp_status svp_stochastic_accept(const void *logits, int64_t row_stri
     if (grid1 < 1)
         grid1 = 1;
     cudaStream_t s = (cudaStream_t)stream;
+    // the acceptance pass is a programmatic dependent of the statistics pass: its CTAs start
+    // on SMs the first pass has left and wait on the device before reading its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n);
+    cfg.blockDim = dim3(kStThreads2);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     if (dtype == SVP_BF16) {
         st_rowstat_kernel<1><<<(unsigned)grid1, kStThreads1, 0, s>>>(p);
-        st_accept_kernel<1><<<n, kStThreads2, 0, s>>>(p);
+        e = cudaGetLastError();
+        if (e == cudaSuccess)
+            e = cudaLaunchKernelEx(&cfg, st_accept_kernel<1>, p);
     } else {
         st_rowstat_kernel<0><<<(unsigned)grid1, kStThreads1, 0, s>>>(p);
-        st_accept_kernel<0><<<n, kStThreads2, 0, s>>>(p);
+        e = cudaGetLastError();
+        if (e == cudaSuccess)
+            e = cudaLaunchKernelEx(&cfg, st_accept_kernel<0>, p);
     }
-    return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
+    return e == cudaSuccess ? SVP_OK : SVP_ECUDA;
 }

@@ -155,6 +155,21 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// Programmatic dependent launch: a grid lets the next grid on its stream (launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization) be scheduled once every one of its
+// CTAs has signalled or exited; the dependent grid waits, before it reads anything the
+// first grid writes, until that grid has completed and its memory is visible.  Without the
+// attribute the wait returns at once.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // L2 cache policies: streamed data is evicted first, reused scratch last.
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
