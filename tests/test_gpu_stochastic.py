@@ -167,3 +167,71 @@ def test_full_size_wide_gqa_sampled_requests():
         if acc[i] != o_acc[0] or nxt[i] != o_nxt[0]:
             assert _borderline(zf, tok[lo:hi], cu1, 1.0, ua[lo:hi], un[i:i + 1], 0, int(nxt[i])), \
                 (i, acc[i], o_acc[0], nxt[i], o_nxt[0])
+
+
+def test_requests_longer_than_a_warp():
+    """Requests of up to 45 slots at a low temperature: the acceptance chain runs past the
+    first 32 candidates (those are loaded before the wait on the statistics pass, the rest
+    after it), with one planted late rejection."""
+    n, V, T = 4, 3000, 0.02
+    z, zf, tok, cu, ua, un = _batch(12, n, V, torch.bfloat16, kmax=45)
+    am = zf.argmax(axis=1)
+    for i in range(n):
+        for j in range(1, int(cu[i + 1] - cu[i])):
+            tok[cu[i] + j] = am[cu[i] + j - 1]
+    big = int(np.argmax(np.diff(cu)))
+    if cu[big + 1] - cu[big] > 40:
+        tok[cu[big] + 40] = (am[cu[big] + 39] + 1) % V   # a late rejection (almost surely)
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    ws = svp.Workspace(svp.stochastic_accept_workspace_size(z.shape[0], V))
+    acc, nxt, pd = svp.stochastic_accept(z.cuda(), d(tok), d(cu), d(ua), d(un), temperature=T, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0
+    o_acc, o_nxt, o_pd = st.stochastic_accept(zf, tok, cu, T, ua.astype(np.float64), un.astype(np.float64))
+    acc, nxt, pd = acc.cpu().numpy(), nxt.cpu().numpy(), pd.cpu().numpy()
+    tested = ~np.isnan(o_pd) & ~np.isnan(pd)
+    assert np.abs(pd[tested] - o_pd[tested]).max() <= TOL
+    assert int(o_acc.max()) > 33   # the chain did go past one warp of candidates
+    for i in range(n):
+        if acc[i] != o_acc[i] or nxt[i] != o_nxt[i]:
+            assert _borderline(zf, tok, cu, T, ua, un, i, int(nxt[i])), (i, acc[i], o_acc[i], nxt[i], o_nxt[i])
+
+
+def test_graph_replay_matches_eager():
+    """The two launches captured in a CUDA graph (the acceptance pass a programmatic
+    dependent of the statistics pass) over two alternating input sets reproduce the eager
+    results bit for bit, replay after replay, on one shared workspace."""
+    n, V = 12, 20000
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    sets = []
+    for seed in (31, 32):
+        z, zf, tok, cu, ua, un = _batch(seed, n, V, torch.bfloat16)
+        sets.append((z.cuda(), d(tok), d(cu), d(ua), d(un)))
+    m_cap = max(s[0].shape[0] for s in sets)
+    ws = svp.Workspace(svp.stochastic_accept_workspace_size(m_cap, V))
+    eager = []
+    for s in sets:
+        r = svp.stochastic_accept(*s, temperature=0.8, ws=ws)
+        eager.append([x.clone() for x in r])
+    torch.cuda.synchronize()
+    outs = [(torch.empty(n, dtype=torch.int32, device="cuda"), torch.empty(n, dtype=torch.int32, device="cuda"),
+             torch.full((s[0].shape[0],), float("nan"), device="cuda")) for s in sets]
+    g = torch.cuda.CUDAGraph()
+    strm = torch.cuda.Stream()
+    strm.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(strm):
+        with torch.cuda.graph(g, stream=strm):
+            for s, o in zip(sets, outs):
+                svp.stochastic_accept(*s, temperature=0.8, ws=ws, outs=o, stream=strm)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for o in outs:
+            o[0].fill_(-7)
+            o[1].fill_(-7)
+            o[2].fill_(float("nan"))   # entries of untested candidates stay unwritten
+        g.replay()
+        torch.cuda.synchronize()
+        for e, o in zip(eager, outs):
+            assert torch.equal(e[0], o[0]) and torch.equal(e[1], o[1])
+            assert torch.equal(torch.nan_to_num(e[2], nan=-1.0), torch.nan_to_num(o[2], nan=-1.0))
+    assert ws.read_status() == 0
