@@ -222,6 +222,8 @@ __device__ void dvl_select(DvlShared &sh, int n_live, int w, bool grow, int32_t 
 
 __global__ void __launch_bounds__(kDvlThreads, 1) dvl_kernel(const DvlParams p)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     extern __shared__ __align__(16) uint8_t dvl_smem[];
     DvlShared &sh = *reinterpret_cast<DvlShared *>(dvl_smem);
     const int tid = threadIdx.x;
@@ -369,6 +371,8 @@ extern "C" svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, i
     // block: every loop of the kernel strides by the block size, and fewer warps meet at
     // each of its barriers
     const int threads = (int64_t)n_bs * w <= kDvlThreads / 4 ? kDvlThreads / 4 : kDvlThreads;
-    dvl_kernel<<<1, threads, sizeof(DvlShared), (cudaStream_t)stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
+    return launch_pdl(dvl_kernel, dim3(1), dim3(threads), sizeof(DvlShared), (cudaStream_t)stream, p) ==
+                   cudaSuccess
+               ? SVP_OK
+               : SVP_ECUDA;
 }

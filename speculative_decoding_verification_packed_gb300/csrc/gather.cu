@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restric
                                                           const int32_t *__restrict__ idx,
                                                           int32_t rows, uint4 *__restrict__ dst)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t total = (int64_t)rows * vecs_per_row;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -45,6 +47,8 @@ struct GatherMulti {
 
 __global__ void __launch_bounds__(256) gather_rows_multi_kernel(const __grid_constant__ GatherMulti g)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t total = g.start[g.n_fields];
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -104,8 +108,10 @@ extern "C" svp_status svp_gather_rows_multi(const svp_gather_field *fields, int3
     const svp_status st = gather_grid(g.start[n_fields], grid);
     if (st != SVP_OK)
         return st;
-    gather_rows_multi_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(g);
-    return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
+    return launch_pdl(gather_rows_multi_kernel, dim3((unsigned)grid), dim3(256), 0, (cudaStream_t)stream, g) ==
+                   cudaSuccess
+               ? SVP_OK
+               : SVP_ECUDA;
 }
 
 extern "C" svp_status svp_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes,
@@ -124,7 +130,9 @@ extern "C" svp_status svp_gather_rows(const void *src, int64_t src_rows, int64_t
     const svp_status st = gather_grid(total, grid);
     if (st != SVP_OK)
         return st;
-    gather_rows_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
-        static_cast<const uint4 *>(src), src_rows, vecs, idx, rows, static_cast<uint4 *>(dst));
-    return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
+    return launch_pdl(gather_rows_kernel, dim3((unsigned)grid), dim3(256), 0, (cudaStream_t)stream,
+                      static_cast<const uint4 *>(src), src_rows, vecs, idx, rows,
+                      static_cast<uint4 *>(dst)) == cudaSuccess
+               ? SVP_OK
+               : SVP_ECUDA;
 }

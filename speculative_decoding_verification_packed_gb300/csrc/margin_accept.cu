@@ -305,6 +305,8 @@ __device__ __forceinline__ int32_t owner_of_row_warp(const int32_t *cu, int32_t 
 template <bool kBf16>
 __global__ void __launch_bounds__(kMarginThreads, 4) margin_kernel(MarginArgs a)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t gwarp = ((int64_t)blockIdx.x * kMarginThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kMarginThreads) >> 5;
@@ -395,6 +397,8 @@ __global__ void greedy_accept_kernel(const int32_t *target_argmax, const int32_t
                                      const int32_t *cu_slots, int32_t n, int32_t m_cap,
                                      int32_t *accept_len, int32_t *next_token, int32_t *status)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n)
         return;
@@ -513,11 +517,10 @@ svp_status margin_launch(const void *logits, int64_t row_stride, int32_t rows, i
         grid = (int64_t)sm_count() * 8;
     if (grid < 1)
         grid = 1;
-    if (dtype == SVP_BF16)
-        margin_kernel<true><<<(unsigned)grid, kMarginThreads, 0, stream>>>(a);
-    else
-        margin_kernel<false><<<(unsigned)grid, kMarginThreads, 0, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
+    const cudaError_t e = dtype == SVP_BF16
+                              ? launch_pdl(margin_kernel<true>, dim3((unsigned)grid), dim3(kMarginThreads), 0, stream, a)
+                              : launch_pdl(margin_kernel<false>, dim3((unsigned)grid), dim3(kMarginThreads), 0, stream, a);
+    return e == cudaSuccess ? SVP_OK : SVP_ECUDA;
 }
 
 svp_status accept_launch(const int32_t *target_argmax, const int32_t *tokens,
@@ -531,9 +534,11 @@ svp_status accept_launch(const int32_t *target_argmax, const int32_t *tokens,
     if (!target_argmax || !tokens || !cu_slots || !accept_len || !next_token)
         return SVP_EINVAL;
     const int threads = 128;
-    greedy_accept_kernel<<<(n + threads - 1) / threads, threads, 0, stream>>>(
-        target_argmax, tokens, cu_slots, n, m_cap, accept_len, next_token, nullptr);
-    return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
+    return launch_pdl(greedy_accept_kernel, dim3((unsigned)((n + threads - 1) / threads)), dim3(threads), 0,
+                      stream, target_argmax, tokens, cu_slots, n, m_cap, accept_len, next_token,
+                      static_cast<int32_t *>(nullptr)) == cudaSuccess
+               ? SVP_OK
+               : SVP_ECUDA;
 }
 
 }  // namespace svp

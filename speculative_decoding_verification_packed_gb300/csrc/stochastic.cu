@@ -625,27 +625,17 @@ extern "C" svp_status svp_stochastic_accept(const void *logits, int64_t row_stri
     cudaStream_t s = (cudaStream_t)stream;
     // the acceptance pass is a programmatic dependent of the statistics pass: its CTAs start
     // on SMs the first pass has left and wait on the device before reading its results
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)n);
-    cfg.blockDim = dim3(kStThreads2);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     cudaError_t e;
     if (dtype == SVP_BF16) {
         st_rowstat_kernel<1><<<(unsigned)grid1, kStThreads1, 0, s>>>(p);
         e = cudaGetLastError();
         if (e == cudaSuccess)
-            e = cudaLaunchKernelEx(&cfg, st_accept_kernel<1>, p);
+            e = launch_pdl(st_accept_kernel<1>, dim3((unsigned)n), dim3(kStThreads2), 0, s, p);
     } else {
         st_rowstat_kernel<0><<<(unsigned)grid1, kStThreads1, 0, s>>>(p);
         e = cudaGetLastError();
         if (e == cudaSuccess)
-            e = cudaLaunchKernelEx(&cfg, st_accept_kernel<0>, p);
+            e = launch_pdl(st_accept_kernel<0>, dim3((unsigned)n), dim3(kStThreads2), 0, s, p);
     }
     return e == cudaSuccess ? SVP_OK : SVP_ECUDA;
 }

@@ -170,6 +170,27 @@ __device__ __forceinline__ void griddep_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Kernels that run in a chain on one stream start with griddep_launch_dependents() and
+// griddep_wait() and are launched this way: each may be scheduled while the one before it
+// finishes (hiding the launch gap and the CTA start-up), and waits on the device before its
+// first read of anything.  Grids launched otherwise behave as plain stream-ordered launches.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // L2 cache policies: streamed data is evicted first, reused scratch last.
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {

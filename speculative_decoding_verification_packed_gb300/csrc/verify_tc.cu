@@ -413,6 +413,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
     int32_t *prefix = reinterpret_cast<int32_t *>(smem + p.off_pref);   // [NQ + 1]
     int32_t *cprefix = prefix + (NQ + 1);                                 // [NQ + 1]
     int32_t *ctile = cprefix + (NQ + 1);                                  // [gridDim.x + 1]
+    // a chained launch: the next kernel may be scheduled from here on; this one reads
+    // nothing before the previous kernel on the stream has completed
+    griddep_launch_dependents();
+    griddep_wait();
     // start the workspace-signature load early; it is checked after the prologue
     const int32_t sig_seen = (tid == 0) ? *reinterpret_cast<volatile int32_t *>(p.status + 1) : 0;
     const int32_t poison_seen =
@@ -1291,8 +1295,10 @@ static svp_status vt_launch_d(const TcParams &p, int grid, cudaStream_t stream)
     static std::atomic<uint64_t> configured{0};
     if (set_smem_limit_once(verify_tc_kernel<D>, 227 * 1024, configured) != cudaSuccess)
         return SVP_ECUDA;
-    verify_tc_kernel<D><<<grid, kVThreads, p.smem_bytes, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? SVP_OK : SVP_ECUDA;
+    return launch_pdl(verify_tc_kernel<D>, dim3(grid), dim3(kVThreads), (size_t)p.smem_bytes, stream, p) ==
+                   cudaSuccess
+               ? SVP_OK
+               : SVP_ECUDA;
 }
 
 svp_status verify_tc_launch(const TcParams &p, int d, int grid, cudaStream_t stream)
