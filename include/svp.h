@@ -39,6 +39,11 @@
  *     never written.
  *   - Kernels never trap.  Every wait inside a kernel is bounded; on expiry the kernel
  *     sets SVP_DEV_TIMEOUT in the status word and returns.
+ *   - The DVL allocator, the row gathers, the verification attention, the margin /
+ *     accept calls and the stochastic verifier's second pass are launched as
+ *     programmatic dependents of the previous kernel on their stream: they may be
+ *     scheduled while it finishes, but read nothing before it has completed, so the
+ *     results are those of plain stream order (also inside a captured CUDA graph).
  */
 #ifndef SVP_H_
 #define SVP_H_
