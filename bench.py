@@ -546,7 +546,7 @@ def run_ours(args):
         extras["prefill_4096_causal"] = prefill_contrast(svp, dev, tf_peak)
         extras.update(next_rows_extras(svp, dev))
         # logit-stream kernels against the same measured HBM copy peak
-        for key in ("stochastic_accept", "draft_features"):
+        for key in ("stochastic_accept", "draft_features", "draft_margin_b2b", "margin_accept_b2b"):
             if key in extras:
                 extras[key]["logit_frac"] = round(extras[key]["logit_gbs"] / hbm_peak, 4)
         result["extras"] = extras
@@ -621,8 +621,9 @@ def graph_us(fn, reps: int = 100, inner: int = 1) -> float:
 
 
 def next_rows_extras(svp, dev):
-    """The allocator/packer, the captured step, the stochastic verifier and the draft
-    features, each timed by graph replay (device time per call)."""
+    """The allocator/packer, the captured step, the stochastic verifier, the draft features
+    and the two margin launches back to back, each timed by graph replay (device time per
+    call)."""
     import numpy as np
     import torch
     from speculative_decoding_verification_packed_gb300 import workloads as wl
@@ -686,27 +687,47 @@ def next_rows_extras(svp, dev):
                             "config": "8 requests, budget 8N = 64 slots, 32q/8kv d=128, ctx U[512,8192], vocab 32000"}
     del pipe, kc, vc
     torch.cuda.empty_cache()
-    # stochastic verifier and draft features on the wide-head workload's logits
-    # two input sets (2 x 207 MB of logits, > L2), calls alternate between them
+    # stochastic verifier, draft features and the two margin launches on the wide-head
+    # workload's logits, back-to-back calls in one graph rotating over three input sets
+    # (2 x 207 MB of logits plus a copy of the first at its own address: no call finds its
+    # logits in the 129 MB L2)
     bs = [wl.make_batch("wide_gqa_bf16", seed=sd, device=dev) for sd in (0, 1)]
     b = bs[0]
     V = b.target_logits.shape[1]
+    lsets = [(bb.draft_logits, bb.target_logits, bb.tokens, bb.cu_slots) for bb in bs]
+    lsets.append((b.draft_logits.clone(), b.target_logits.clone(), b.tokens, b.cu_slots))
     ua = torch.rand(b.m_cap, device=dev)
     un = torch.rand(b.n, device=dev)
     wss = svp.Workspace(svp.stochastic_accept_workspace_size(b.m_cap, V), dev)
     souts = (torch.empty(b.n, dtype=torch.int32, device=dev), torch.empty(b.n, dtype=torch.int32, device=dev),
              torch.empty(b.m_cap, dtype=torch.float32, device=dev))
-    us = graph_us([lambda bb=bb: svp.stochastic_accept(bb.target_logits, bb.tokens, bb.cu_slots, ua, un,
-                                                       temperature=1.0, ws=wss, outs=souts) for bb in bs])
+    us = graph_us([lambda ls=ls: svp.stochastic_accept(ls[1], ls[2], ls[3], ua, un, temperature=1.0, ws=wss,
+                                                       outs=souts) for ls in lsets])
     tb = int(b.cu_slots[-1]) * V * 2
     out["stochastic_accept"] = {"us": round(us, 2), "logit_gbs": round(tb / (us / 1e6) / 1e9, 1),
-                                "config": "224 target rows x 248320 bf16, T = 1, 2 alternating input sets"}
+                                "config": "224 target rows x 248320 bf16, T = 1, 3 alternating input sets"}
     wsf = svp.Workspace(svp.draft_features_workspace_size(b.draft_logits.shape[0], V), dev)
     fout = torch.empty(b.draft_logits.shape[0], 18, dtype=torch.float32, device=dev)
-    us = graph_us([lambda bb=bb: svp.draft_features(bb.draft_logits, ws=wsf, out=fout) for bb in bs])
+    us = graph_us([lambda ls=ls: svp.draft_features(ls[0], ws=wsf, out=fout) for ls in lsets])
     db = b.draft_logits.numel() * 2
     out["draft_features"] = {"us": round(us, 2), "logit_gbs": round(db / (us / 1e6) / 1e9, 1),
-                             "config": "192 draft rows x 248320 bf16, 18 values per row, 2 alternating input sets"}
+                             "config": "192 draft rows x 248320 bf16, 18 values per row, 3 alternating input sets"}
+    # the two margin launches of the wide-head step timed the same way; the step's
+    # per-launch events (wide_gqa_bf16 extras) also charge each launch its start-up gap
+    wsd = svp.Workspace(svp.draft_margin_workspace_size(b.draft_logits.shape[0], V), dev)
+    dout = tuple(torch.empty(b.draft_logits.shape[0], dtype=t, device=dev)
+                 for t in (torch.int32, torch.float32, torch.float32, torch.float32))
+    us = graph_us([lambda ls=ls: svp.draft_margin(ls[0], ws=wsd, outs=dout) for ls in lsets])
+    out["draft_margin_b2b"] = {"us": round(us, 2), "logit_gbs": round(db / (us / 1e6) / 1e9, 1),
+                               "config": "192 draft rows x 248320 bf16, back-to-back calls, 3 alternating input sets"}
+    wsm = svp.Workspace(svp.margin_accept_workspace_size(b.n, b.m_cap, V), dev)
+    mout = tuple(torch.empty(b.m_cap, dtype=t, device=dev) for t in (torch.int32, torch.float32, torch.float32,
+                                                                      torch.float32)) + \
+        (torch.empty(b.n, dtype=torch.int32, device=dev), torch.empty(b.n, dtype=torch.int32, device=dev))
+    us = graph_us([lambda ls=ls: svp.margin_accept(ls[1], ls[2], ls[3], ws=wsm, outs=mout) for ls in lsets])
+    out["margin_accept_b2b"] = {"us": round(us, 2), "logit_gbs": round(tb / (us / 1e6) / 1e9, 1),
+                                "config": "224 target rows x 248320 bf16 + greedy accept, back-to-back calls, "
+                                          "3 alternating input sets"}
     return out
 
 
