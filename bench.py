@@ -528,6 +528,11 @@ def run_ours(args):
                  "kv_gbs": round(okv / (opl["attn"] / 1e3) / 1e9, 1),
                  "kv_frac": round(okv / (opl["attn"] / 1e3) / 1e9 / hbm_peak, 4),
                  "per_launch_us": {k: round(v * 1e3, 2) for k, v in opl.items()}}
+            # the attention launch also timed back to back (device time per call of a graph of
+            # calls rotating over the sets); the step's events charge each launch its start-up gap
+            bus = graph_us([dict(build_step(bb, svp)[0])["attn"] for bb in osets])
+            e["attn_b2b_us"] = round(bus, 2)
+            e["kv_frac_b2b"] = round(okv / (bus / 1e6) / 1e9 / hbm_peak, 4)
             fms, fpl, _, _, _ = timed_run(osets, st, 3, svp, tile_mode=svp.TILE_FIXED128)
             e["fixed128_rows_per_s"] = round(orows / (fms / 1e3), 1)
             ums, upl, _, _, _ = timed_run(osets, st, 3, svp, tile_mode=svp.TILE_SHORT_UNPACKED)
@@ -636,8 +641,10 @@ def next_rows_extras(svp, dev):
         rng = np.random.default_rng(n)
         sc = rng.beta(2.0, 1.2, (n, 15)).astype(np.float32)
         s_t = torch.from_numpy(sc).to(dev)
-        tok = torch.randint(0, 150000, (n, 16), dtype=torch.int32, device=dev)
-        pos = torch.randint(0, 1 << 20, (n, 16), dtype=torch.int32, device=dev)
+        gd = torch.Generator(device=dev)
+        gd.manual_seed(n)
+        tok = torch.randint(0, 150000, (n, 16), dtype=torch.int32, device=dev, generator=gd)
+        pos = torch.randint(0, 1 << 20, (n, 16), dtype=torch.int32, device=dev, generator=gd)
         ws = svp.Workspace(256, dev)
         holder = {}
 
@@ -660,18 +667,21 @@ def next_rows_extras(svp, dev):
     out["dvl_allocate_pack"] = dv
     # captured step: allocate/pack, gather, verify (full-width shapes), margin + accept
     n_bs, V = 8, 32000
-    ctx = torch.randint(512, 8193, (n_bs,), dtype=torch.int32)
+    gc = torch.Generator().manual_seed(7)
+    gd = torch.Generator(device=dev)
+    gd.manual_seed(7)
+    ctx = torch.randint(512, 8193, (n_bs,), dtype=torch.int32, generator=gc)
     cu_ctx = torch.zeros(n_bs + 1, dtype=torch.int64)
     cu_ctx[1:] = torch.cumsum(ctx.long(), 0)
-    kc = torch.randn(int(cu_ctx[-1]), 8, 128, device=dev).to(torch.bfloat16)
-    vc = torch.randn(int(cu_ctx[-1]), 8, 128, device=dev).to(torch.bfloat16)
+    kc = torch.randn(int(cu_ctx[-1]), 8, 128, device=dev, generator=gd).to(torch.bfloat16)
+    vc = torch.randn(int(cu_ctx[-1]), 8, 128, device=dev, generator=gd).to(torch.bfloat16)
     pipe = VerifyPipeline(n_bs, hq=32, hkv=8, d=128, vocab=V, ctx_len=ctx.to(dev),
                           kv_tensors=dict(k_ctx=kc, v_ctx=vc, cu_ctx=cu_ctx.to(dev)))
-    pipe.scores.copy_(torch.rand(n_bs, 15, device=dev))
-    pipe.q_full.normal_()
-    pipe.k_full.normal_()
-    pipe.v_full.normal_()
-    pipe.logits_full.normal_()
+    pipe.scores.copy_(torch.rand(n_bs, 15, device=dev, generator=gd))
+    pipe.q_full.normal_(generator=gd)
+    pipe.k_full.normal_(generator=gd)
+    pipe.v_full.normal_(generator=gd)
+    pipe.logits_full.normal_(generator=gd)
     pipe.capture()
     for _ in range(3):
         pipe.step()
@@ -696,8 +706,10 @@ def next_rows_extras(svp, dev):
     V = b.target_logits.shape[1]
     lsets = [(bb.draft_logits, bb.target_logits, bb.tokens, bb.cu_slots) for bb in bs]
     lsets.append((b.draft_logits.clone(), b.target_logits.clone(), b.tokens, b.cu_slots))
-    ua = torch.rand(b.m_cap, device=dev)
-    un = torch.rand(b.n, device=dev)
+    gu = torch.Generator(device=dev)
+    gu.manual_seed(11)
+    ua = torch.rand(b.m_cap, device=dev, generator=gu)
+    un = torch.rand(b.n, device=dev, generator=gu)
     wss = svp.Workspace(svp.stochastic_accept_workspace_size(b.m_cap, V), dev)
     souts = (torch.empty(b.n, dtype=torch.int32, device=dev), torch.empty(b.n, dtype=torch.int32, device=dev),
              torch.empty(b.m_cap, dtype=torch.float32, device=dev))
