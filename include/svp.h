@@ -31,7 +31,9 @@
  *     number of requests, m_cap and w may change from call to call (re-query the size:
  *     it grows with n); the attention workspace is tied to one head_dim and tile mode
  *     (a mismatch is reported as SVP_DEV_WORKSPACE and nothing is computed).  Kernels
- *     leave their counters at zero when they finish.  Calls that share one workspace
+ *     leave their counters and per-call scratch at zero when they finish (the attention
+ *     kernel's partial slots sit at size-independent offsets before its counters), so a
+ *     workspace serves later calls of any size.  Calls that share one workspace
  *     must not overlap on the GPU.  After SVP_DEV_TIMEOUT, zero the workspace again:
  *     until then an attention call on it computes nothing and reports SVP_DEV_WORKSPACE
  *     (its split-KV tickets may have been left mid-count).
@@ -351,8 +353,9 @@ svp_status svp_stochastic_accept_workspace_size(int32_t m_cap, int32_t vocab, si
  * (the acceptance probability of each tested candidate; may be NULL).  Rows >=
  * cu_slots[n] are not read.  Invalid cu_slots (cu_slots[0] != 0, a decrease, or
  * cu_slots[n] > m_cap) set SVP_DEV_BAD_SLOTS: no row is read and every request gets
- * accept_len 0 and next_token -1.  ws zeroed once (svp_workspace_init); the kernel leaves
- * its tickets at zero.
+ * accept_len 0 and next_token -1.  ws zeroed once (svp_workspace_init); the kernels leave
+ * it zeroed (tickets, row and chunk statistics), so it can serve later calls with other
+ * m_cap and vocabularies.
  */
 svp_status svp_stochastic_accept(const void *logits, int64_t row_stride, int32_t m_cap,
                                  int32_t vocab, svp_dtype dtype, const int32_t *tokens,
@@ -372,7 +375,8 @@ svp_status svp_draft_features_workspace_size(int32_t rows, int32_t vocab, size_t
 
 /*
  * logits [rows, row_stride] (dtype), 16 <= vocab <= row_stride; features [rows, 18] fp32.
- * ws zeroed once (svp_workspace_init); the kernel leaves its tickets at zero.
+ * ws zeroed once (svp_workspace_init); the kernel leaves it zeroed (tickets and partial
+ * lists), so it can serve later calls with other row counts and vocabularies.
  */
 svp_status svp_draft_features(const void *logits, int64_t row_stride, int32_t rows,
                               int32_t vocab, svp_dtype dtype, float *features, void *ws,

@@ -617,6 +617,12 @@ __global__ void __launch_bounds__(kFtThreads, 3) features_kernel(const FtParams 
             }
             ft_stat_warp(ms);
             ft_write(p, r, mg, ms, lane);
+            // the row's partials go back to zero with its ticket: the workspace is all zero
+            // after every call, so it can serve later calls with other row counts and vocabularies
+            __syncwarp();   // every lane's reads of them first
+            float *rp = p.partial + (int64_t)r * p.chunks * kFtPart;
+            for (int32_t x = lane; x < p.chunks * kFtPart; x += 32)
+                rp[x] = 0.0f;
             if (lane == 0)
                 p.tickets[r] = 0;
         }

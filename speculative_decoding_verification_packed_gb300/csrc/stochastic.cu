@@ -393,6 +393,14 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
         }
     }
     __syncthreads();
+    // the request's rows are done with their statistics: back to zero, so that the workspace
+    // is all zero after every call and serves later calls with other m_cap and vocabularies
+    for (int32_t x = tid; x < k * (1 + p.chunks); x += kStThreads2) {
+        if (x < k)
+            p.row_stat[off + x] = make_float2(0.0f, 0.0f);
+        else
+            p.partial[(int64_t)off * p.chunks + (x - k)] = make_float2(0.0f, 0.0f);
+    }
     const int32_t r = sh_row, excl = sh_excl, ch = sh_chunk;
     if (ch < 0) {   // no token with weight at all (every other token underflowed)
         if (tid == 0)

@@ -112,3 +112,22 @@ def test_features_several_units_per_warp(rows, V, pad):
     assert np.all(np.abs(out[:, 1:16] - ref[:, 1:16]) <= 6e-8 * np.maximum(np.abs(ref[:, 1:16]), np.abs(ref[:, :1])))
     assert np.abs(out[:, 16] - ref[:, 16]).max() <= 1e-4
     assert np.abs(out[:, 17] - ref[:, 17]).max() <= 1e-4 * np.log(V)
+
+
+def test_workspace_reused_across_sizes():
+    """One workspace, sized for the largest call, serves calls with other row counts and
+    vocabularies: every call leaves it zeroed, so no stale partial list lands in a later
+    call's row tickets (the layout moves with the row count)."""
+    shapes = [(232, 60000, torch.bfloat16), (270, 4099, torch.float32), (17, 1001, torch.float32),
+              (300, 20000, torch.bfloat16), (40, 248320, torch.bfloat16)]
+    ws = svp.Workspace(max(svp.draft_features_workspace_size(r, V) for r, V, _ in shapes))
+    for i, (rows, V, dtype) in enumerate(shapes):
+        g = torch.Generator().manual_seed(50 + i)
+        z = (torch.randn(rows, V, generator=g) * 2.0).to(dtype)
+        ref = ft.draft_features(z.float().numpy().astype(np.float64))
+        out = svp.draft_features(z.cuda(), ws=ws).cpu().numpy().astype(np.float64)
+        assert out[:, 0].tolist() == ref[:, 0].tolist(), (rows, V)
+        assert np.all(np.abs(out[:, 1:16] - ref[:, 1:16]) <= 6e-8 * np.maximum(np.abs(ref[:, 1:16]), np.abs(ref[:, :1])))
+        assert np.abs(out[:, 16] - ref[:, 16]).max() <= 1e-4
+        assert np.abs(out[:, 17] - ref[:, 17]).max() <= 1e-4 * np.log(V)
+    assert torch.count_nonzero(ws.buf[256:]).item() == 0   # all zero again past the header

@@ -1,11 +1,13 @@
-"""GPU parity on seeded random configurations: verification attention and fused margin +
-accept against the fp64 oracle.
+"""GPU parity on seeded random configurations against the fp64 oracle: verification
+attention, fused margin + accept, the stochastic prefix verifier and the draft features.
 
 Each case draws its shape at random (fixed seeds, so every run checks the same cases): the
 number of requests, their slot counts (0 = inactive, up to 16) and context lengths (0 to
 a few thousand, ending anywhere within a 128-key tile or a 16-token page), the head dim
 (128 or 256), the query heads per KV head (1 to 12), contiguous or paged context, and the
 tile mode.  Packed tail rows are poisoned with NaN and must stay unread and unwritten.
+The logit-row cases draw the vocabulary, a padded row stride, the dtype and the value
+scale, with empty requests, tie-heavy rows and rows with -inf entries.
 """
 import numpy as np
 import pytest
@@ -81,3 +83,78 @@ def test_random_margin_accept_configs(seed):
                                     tokens, cu)
     assert np.array_equal(outs[4].cpu().numpy(), acc)
     assert np.array_equal(outs[5].cpu().numpy(), nxt)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_stochastic_configs(seed):
+    """Stochastic prefix verifier on random shapes: request count and lengths (empty ones
+    included), vocabulary (2 to 151,936, odd sizes), padded row stride, dtype and
+    temperature; decisions exact unless within rounding of their boundary, acceptance
+    probabilities to the same bar as the fixed cases."""
+    from oracle import stochastic as st
+    from test_gpu_stochastic import TOL, _borderline
+    rng = np.random.default_rng(3000 + seed)
+    n = int(rng.integers(1, 25))
+    V = [2, 17, 1000, 32000, 151936, 4099][seed]
+    pad = int(rng.integers(0, 10))
+    dtype = torch.float32 if seed in (1, 4) else torch.bfloat16
+    T = float(rng.choice([0.3, 0.7, 1.0, 2.0]))
+    ks = rng.integers(0, 21, n)
+    cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    m = max(int(cu[-1]) + int(rng.integers(0, 4)), 1)
+    g = torch.Generator().manual_seed(seed)
+    z = (torch.randn(m, V + pad, generator=g) * float(rng.choice([1.0, 2.0, 4.0]))).to(dtype)
+    zf = z.float().numpy()[:, :V].astype(np.float64)
+    am = zf.argmax(axis=1)
+    tok = rng.integers(0, V, m).astype(np.int32)
+    for i in range(n):
+        for j in range(1, int(ks[i])):
+            if rng.random() < 0.6:
+                tok[cu[i] + j] = am[cu[i] + j - 1]
+    ua = rng.random(m).astype(np.float32)
+    un = rng.random(n).astype(np.float32)
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    ws = svp.Workspace(svp.stochastic_accept_workspace_size(m, V))
+    acc, nxt, pd = svp.stochastic_accept(z.cuda(), d(tok), d(cu), d(ua), d(un), temperature=T, vocab=V, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0
+    o_acc, o_nxt, o_pd = st.stochastic_accept(zf, tok, cu, T, ua.astype(np.float64), un.astype(np.float64))
+    acc, nxt, pd = acc.cpu().numpy(), nxt.cpu().numpy(), pd.cpu().numpy()
+    tested = ~np.isnan(o_pd) & ~np.isnan(pd)
+    assert np.abs(pd[tested] - o_pd[tested]).max(initial=0.0) <= TOL
+    for i in range(n):
+        if acc[i] != o_acc[i] or nxt[i] != o_nxt[i]:
+            assert _borderline(zf, tok, cu, T, ua, un, i, int(nxt[i])), (i, acc[i], o_acc[i], nxt[i], o_nxt[i])
+    assert set(np.where(ks == 0)[0].tolist()) <= set(np.where(acc == 0)[0].tolist())
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_features_configs(seed):
+    """Draft features on random shapes: rows (1 to 300), vocabulary (16 to 60,000, odd sizes),
+    padded row stride, dtype, value scale, rows quantised to a coarse grid (many ties) and
+    rows with up to a third of their entries -inf."""
+    from oracle import features as ft
+    rng = np.random.default_rng(4000 + seed)
+    rows = int(rng.integers(1, 301))
+    V = [16, 100, 4097, 32000, 60000, 4099][seed]
+    pad = int(rng.integers(0, 10))
+    dtype = torch.float32 if seed in (2, 5) else torch.bfloat16
+    g = torch.Generator().manual_seed(100 + seed)
+    z = torch.randn(rows, V + pad, generator=g) * float(rng.choice([0.5, 2.0, 8.0]))
+    for r in range(rows):
+        u = rng.random()
+        if u < 0.15:
+            z[r] = torch.round(z[r] * 2.0) / 2.0              # coarse grid: many equal values
+        elif u < 0.3 and V >= 64:
+            cut = torch.from_numpy(rng.random(V + pad) < rng.random() / 3)
+            z[r][cut] = -float("inf")
+    z = z.to(dtype)
+    ref = ft.draft_features(z.float().numpy()[:, :V].astype(np.float64))
+    out = svp.draft_features(z.cuda(), vocab=V).cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref[:, 1:16])
+    assert out[:, 0].tolist() == ref[:, 0].tolist()
+    assert np.array_equal(np.isfinite(out[:, 1:16]), fin)
+    dd = np.abs(np.where(fin, out[:, 1:16], 0.0) - np.where(fin, ref[:, 1:16], 0.0))
+    assert np.all(dd <= 6e-8 * np.maximum(np.abs(np.where(fin, ref[:, 1:16], 0.0)), np.abs(ref[:, :1])))
+    assert np.abs(out[:, 16] - ref[:, 16]).max() <= 1e-4
+    assert np.abs(out[:, 17] - ref[:, 17]).max() <= 1e-4 * max(1.0, np.log(V))

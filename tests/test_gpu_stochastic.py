@@ -235,3 +235,27 @@ def test_graph_replay_matches_eager():
             assert torch.equal(e[0], o[0]) and torch.equal(e[1], o[1])
             assert torch.equal(torch.nan_to_num(e[2], nan=-1.0), torch.nan_to_num(o[2], nan=-1.0))
     assert ws.read_status() == 0
+
+
+def test_workspace_reused_across_sizes():
+    """One workspace, sized for the largest call, serves calls with other m_cap and
+    vocabularies: every call leaves it zeroed (tickets, row and chunk statistics), so no
+    stale statistic lands in a later call's row tickets (the layout moves with m_cap)."""
+    cases = [(30, 1000, torch.bfloat16), (8, 32000, torch.bfloat16), (40, 3000, torch.float32),
+             (4, 151936, torch.bfloat16), (25, 500, torch.bfloat16)]
+    batches = [_batch(60 + i, n, V, dtype) for i, (n, V, dtype) in enumerate(cases)]
+    ws = svp.Workspace(max(svp.stochastic_accept_workspace_size(b[0].shape[0], V)
+                           for b, (_, V, _) in zip(batches, cases)))
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    for (n, V, dtype), (z, zf, tok, cu, ua, un) in zip(cases, batches):
+        acc, nxt, pd = svp.stochastic_accept(z.cuda(), d(tok), d(cu), d(ua), d(un), temperature=1.0, ws=ws)
+        torch.cuda.synchronize()
+        assert ws.read_status() == 0
+        o_acc, o_nxt, o_pd = st.stochastic_accept(zf, tok, cu, 1.0, ua.astype(np.float64), un.astype(np.float64))
+        acc, nxt, pd = acc.cpu().numpy(), nxt.cpu().numpy(), pd.cpu().numpy()
+        tested = ~np.isnan(o_pd) & ~np.isnan(pd)
+        assert np.abs(pd[tested] - o_pd[tested]).max(initial=0.0) <= TOL
+        for i in range(n):
+            if acc[i] != o_acc[i] or nxt[i] != o_nxt[i]:
+                assert _borderline(zf, tok, cu, 1.0, ua, un, i, int(nxt[i])), (n, V, i)
+        assert torch.count_nonzero(ws.buf[256:]).item() == 0   # all zero again past the header
