@@ -1,5 +1,6 @@
 """GPU parity on seeded random configurations against the fp64 oracle: verification
-attention, fused margin + accept, the stochastic prefix verifier and the draft features.
+attention (short tile, wide tile for blocks wider than 16, fp32 CUDA-core path), fused
+margin + accept, the stochastic prefix verifier and the draft features.
 
 Each case draws its shape at random (fixed seeds, so every run checks the same cases): the
 number of requests, their slot counts (0 = inactive, up to 16) and context lengths (0 to
@@ -158,3 +159,54 @@ def test_random_features_configs(seed):
     assert np.all(dd <= 6e-8 * np.maximum(np.abs(np.where(fin, ref[:, 1:16], 0.0)), np.abs(ref[:, :1])))
     assert np.abs(out[:, 16] - ref[:, 16]).max() <= 1e-4
     assert np.abs(out[:, 17] - ref[:, 17]).max() <= 1e-4 * max(1.0, np.log(V))
+
+
+_WIDE_HEADS = [(4, 2), (8, 8), (6, 1), (16, 4), (2, 2), (12, 4)]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_wide_configs(seed):
+    """Candidate blocks wider than 16 (the router's 128-row wide tile): request count, block
+    width 17 to 199, slot counts (0 included), context lengths, head dim 64 / 128 / 256,
+    query heads per KV head, contiguous or paged context."""
+    rng = np.random.default_rng(5000 + seed)
+    d = [64, 128, 256][seed % 3]
+    hq, hkv = _WIDE_HEADS[seed]
+    n = int(rng.integers(1, 5))
+    W = int(rng.integers(17, 200))
+    lengths = [int(x) for x in rng.integers(0, W + 1, size=n)]
+    if sum(lengths) == 0:
+        lengths[0] = W
+    ctx = [int(x) if rng.random() < 0.8 else 0 for x in rng.integers(1, 2500, size=n)]
+    paged = bool(rng.random() < 0.5)
+    b = wl.make_batch("paged_n64_bf16" if paged else "budget8n_bf16", seed=seed, n=n, W=W,
+                      lengths=lengths, ctx_lengths=ctx, hq=hq, hkv=hkv, d=d, poison=True,
+                      with_logits=False)
+    out, lse = gpu_verify(to_dev(b), w=W)
+    ref_o, ref_l = oracle_verify(b)
+    compare_attention(out, lse, ref_o, ref_l, rows_of(b), torch.bfloat16)
+    assert torch.isnan(out[b.m_live:].float()).all()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_fp32_configs(seed):
+    """fp32 inputs (the CUDA-core path): random request count, block width up to 40, slot
+    counts, context lengths, head dim 64 / 128 / 256, query heads per KV head, contiguous or
+    paged context; to the fp32 bar."""
+    rng = np.random.default_rng(6000 + seed)
+    d = [64, 128, 256, 128][seed]
+    hq, hkv = [(4, 2), (8, 1), (3, 3), (12, 4)][seed]
+    n = int(rng.integers(1, 6))
+    W = int(rng.integers(1, 41))
+    lengths = [int(x) for x in rng.integers(0, W + 1, size=n)]
+    if sum(lengths) == 0:
+        lengths[0] = W
+    ctx = [int(x) if rng.random() < 0.8 else 0 for x in rng.integers(1, 1200, size=n)]
+    paged = bool(rng.random() < 0.5)
+    b = wl.make_batch("paged_n64_bf16" if paged else "budget8n_bf16", seed=seed, n=n, W=W,
+                      lengths=lengths, ctx_lengths=ctx, hq=hq, hkv=hkv, d=d, dtype="f32",
+                      poison=True, with_logits=False)
+    out, lse = gpu_verify(to_dev(b), w=W)
+    ref_o, ref_l = oracle_verify(b)
+    compare_attention(out, lse, ref_o, ref_l, rows_of(b), torch.float32)
+    assert torch.isnan(out[b.m_live:].float()).all()
