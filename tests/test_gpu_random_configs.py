@@ -1,6 +1,6 @@
 """GPU parity on seeded random configurations against the fp64 oracle: verification
-attention (short tile, wide tile for blocks wider than 16, fp32 CUDA-core path), fused
-margin + accept, the stochastic prefix verifier and the draft features.
+attention (short tile, wide tile for blocks wider than 16, fp32 CUDA-core path), causal
+prefill, fused margin + accept, the stochastic prefix verifier and the draft features.
 
 Each case draws its shape at random (fixed seeds, so every run checks the same cases): the
 number of requests, their slot counts (0 = inactive, up to 16) and context lengths (0 to
@@ -210,3 +210,35 @@ def test_random_fp32_configs(seed):
     ref_o, ref_l = oracle_verify(b)
     compare_attention(out, lse, ref_o, ref_l, rows_of(b), torch.float32)
     assert torch.isnan(out[b.m_live:].float()).all()
+
+
+_PREFILL_HEADS = [(4, 2, 128), (8, 2, 128), (8, 4, 128), (6, 2, 128), (4, 2, 64)]
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_random_prefill_configs(seed):
+    """Causal prefill on random packed sequences: 1 to 8 sequences of 0 to 800 rows (on and off
+    the 128-row tile); even query-head groups at d = 128 take the dedicated kernel, an odd
+    group or d = 64 the general one."""
+    import oracle
+    rng = np.random.default_rng(7000 + seed)
+    hq, hkv, d = _PREFILL_HEADS[seed]
+    n = int(rng.integers(1, 9))
+    lens = [int(x) for x in rng.integers(0, 801, size=n)]
+    lens[int(rng.integers(n))] = int(rng.choice([1, 128, 256, 513]))
+    if seed == 2:
+        lens.insert(1, 0)   # an empty sequence between two others
+        n += 1
+    parts = [wl.make_prefill(seed=100 * seed + i, s=max(L, 1), hq=hq, hkv=hkv, d=d) for i, L in enumerate(lens)]
+    q = torch.cat([x[0][:L] for x, L in zip(parts, lens)])
+    k = torch.cat([x[1][:L] for x, L in zip(parts, lens)])
+    v = torch.cat([x[2][:L] for x, L in zip(parts, lens)])
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    ws = svp.Workspace(svp.prefill_attn_workspace_size(n, max(max(lens), 1), hq, hkv, d))
+    out, lse = svp.prefill_attn(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), max_s=max(max(lens), 1), ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0
+    ref_o, ref_l = oracle.attention(q, k, v, torch.zeros(n, dtype=torch.int32), cu, hkv=hkv,
+                                    scale=d ** -0.5, k_ctx=k[:0], v_ctx=v[:0],
+                                    cu_ctx=torch.zeros(n + 1, dtype=torch.int64), threads=16)
+    compare_attention(out, lse, ref_o, ref_l, np.arange(int(cu[-1])), torch.bfloat16)
