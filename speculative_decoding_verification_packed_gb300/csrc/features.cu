@@ -8,20 +8,26 @@
 //
 // Row reduction over (row, chunk) units, one warp per unit, the chunk sized so that the
 // units fill the GPU's resident warps once; the chunks of a row are merged by the last warp
-// to take the row's ticket.
+// to take the row's acquire-release ticket, which also returns the row's partial lists and
+// ticket to zero (the workspace is all zero after every call).
 //  * Softmax statistics per lane: an online (max m, s = sum 2^d, t = sum 2^d d) with
-//    d = (z - m) log2 e; entropy = ln s - t ln2 / s, log-sum-exp = m + ln s.  bf16 rows
-//    rebase (m, s, t) once per full batch of eight 16-byte vectors (batch maximum by packed
-//    max).
+//    d = (z - m) log2 e; entropy = ln s - t ln2 / s, log-sum-exp = m + ln s.  bf16 rows:
+//    a batch of eight 16-byte vectors is summed in packed f32x2 arithmetic against the
+//    running reference m, which then moves to the batch maximum; a batch whose sums
+//    overflow or turn NaN (a -inf logit) is redone with the reference moved first and -inf
+//    read as -9.97e37.  A warp's (m, s, t) fold: the warp maximum by one redux, one rescale
+//    per lane, a butterfly sum.
 //  * Top-16, bf16 rows: each lane's 8 streams (packed word k of its 16-byte vectors, low or
-//    high half) keep their top 4 with packed bf16 min / max, branch-free; 16 rounds of warp
-//    maximum draw the chunk's top-16 from those entries.  Exact unless a stream's fourth
-//    value reaches the 16th drawn value; then (rarely) the chunk is rescanned taking only
-//    values at or above it.
+//    high half) keep their top 4; a selection network on the packed words merges each
+//    batch's 8 values per stream (and yields the batch maximum).  16 rounds of redux on
+//    unique order-preserving keys draw the chunk's top-16 from those entries.  Exact unless
+//    a stream's fourth value reaches the 16th drawn value; then (rarely) the chunk is
+//    rescanned taking only values at or above it.
 //  * Top-16, fp32 rows and the rescan: the warp's top-16 so far sorted across lanes 0..15
 //    with the 16th value as a warp-uniform threshold; a vector is offered only when its
 //    maximum beats the threshold, and an insertion is a ballot, a popcount and a lane shift.
-// HBM-bound over rows x vocab.
+// HBM-bound over rows x vocab (issue-bound in practice for bf16: packed min / max and one
+// exponential per value).
 #include <cstdint>
 #include <cuda_runtime.h>
 

@@ -18,7 +18,10 @@
 // while the other warps bring the chunk statistics of the request's rows into shared
 // memory, then walks the chunk masses of the successor row in token order to the chunk
 // that holds the draw; the block rescans only that chunk (block prefix sum of per-thread
-// masses, then one thread's elements in order).
+// masses, then one thread's elements in order).  (2) is a programmatic dependent launch of
+// (1): its blocks start on SMs that (1) has left, load their input-only operands, and wait
+// on the device before reading the statistics; each block returns its request's row and
+// chunk statistics to zero once read, so the workspace is all zero after every call.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
