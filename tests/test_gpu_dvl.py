@@ -81,13 +81,34 @@ def test_random_batches_match_reference(seed):
 
 
 @pytest.mark.parametrize("w", [2, 5, 16])
-def test_widths_and_extremes(w):
+@pytest.mark.parametrize("n", [20, 40])   # a quarter block and a full block of threads
+def test_widths_and_extremes(w, n):
     rng = np.random.default_rng(w)
-    n = 40
     for s in (np.ones((n, w - 1)), np.zeros((n, w - 1)), rng.random((n, w - 1))):
         for per in sorted({1, max(1, w // 2), w}):
             g, o, ws = _run(s.astype(np.float32), n, per, w * n + 5, seed=w)
             _assert_same(g, o)
+
+
+@pytest.mark.parametrize("n_bs", [1, 2, 17, 31, 32, 33])
+def test_small_batch_sizes(n_bs):
+    """Small batches (fewer requests than a warp, about one warp, one more): the kernel
+    agrees with the reference on growing, shrinking and tie-heavy batches, with all, some
+    or none of the requests live."""
+    rng = np.random.default_rng(500 + n_bs)
+    for kind in range(3):
+        if kind == 0:
+            s = rng.random((n_bs, 15))
+        elif kind == 1:
+            s = rng.integers(0, 3, (n_bs, 15)) / 2.0      # few distinct values: many ties
+        else:
+            s = rng.beta(0.3, 0.3, (n_bs, 15))
+        s = s.astype(np.float32)
+        for n_live in sorted({n_bs, max(0, n_bs - 3), 0}):
+            for per in (1, 4, 16):
+                g, o, ws = _run(s, n_live, per, 16 * n_bs + 2, seed=kind)
+                _assert_same(g, o)
+                assert ws.read_status() == 0
 
 
 def test_no_fields_and_bad_live_count():
