@@ -414,7 +414,9 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
     const int64_t rowb = (int64_t)r * p.row_stride;
     const int64_t clo = (int64_t)ch * p.chunk;
     const int64_t chi = clo + p.chunk < p.vocab ? clo + p.chunk : p.vocab;
-    // per thread a contiguous run of whole 16-byte vectors (the chunk starts on one)
+    // per thread a contiguous run of whole 16-byte vectors (the chunk starts on one); each
+    // weight is one ex2.approx (relative error ~2^-22), the same expression in the sum below
+    // and in the claiming thread's scan, so that the scan reproduces the sum exactly
     constexpr int VEC = DT == 1 ? 8 : 4;
     const int64_t per = ((chi - clo + kStThreads2 - 1) / kStThreads2 + VEC - 1) / VEC * VEC;
     const int64_t lo = clo + (int64_t)tid * per;
@@ -442,10 +444,10 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
                 for (int h = 0; h < 4; ++h) {
                     if (DT == 1) {
                         const int64_t e2 = lo + v * VEC + 2 * h;
-                        own += e2 != excl ? exp2f((bf16_lo(w[h]) - m) * p.c) : 0.0f;
-                        own += e2 + 1 != excl ? exp2f((bf16_hi(w[h]) - m) * p.c) : 0.0f;
+                        own += e2 != excl ? fast_exp2((bf16_lo(w[h]) - m) * p.c) : 0.0f;
+                        own += e2 + 1 != excl ? fast_exp2((bf16_hi(w[h]) - m) * p.c) : 0.0f;
                     } else {
-                        own += lo + v * VEC + h != excl ? exp2f((__uint_as_float(w[h]) - m) * p.c) : 0.0f;
+                        own += lo + v * VEC + h != excl ? fast_exp2((__uint_as_float(w[h]) - m) * p.c) : 0.0f;
                     }
                 }
             }
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
     }
     for (; e < hi; ++e)
         if (e != excl)
-            own += exp2f((st_load<DT>(p.logits, rowb + e) - m) * p.c);
+            own += fast_exp2((st_load<DT>(p.logits, rowb + e) - m) * p.c);
     // block exclusive scan of the per-thread masses
     float incl = own;
 #pragma unroll
@@ -499,7 +501,7 @@ __global__ void __launch_bounds__(kStThreads2) st_accept_kernel(const StParams p
         auto take = [&](int64_t e2, float v) {
             if (found || e2 == excl)
                 return;
-            const float w = exp2f((v - m) * p.c);
+            const float w = fast_exp2((v - m) * p.c);
             if (w > 0.0f)
                 lnz = (int32_t)e2;
             cum += w;
