@@ -309,3 +309,27 @@ def test_one_long_pair_split_over_many_ctas(paged, d, hq, k):
     out, lse = gpu_verify(to_dev(b))
     ref_o, ref_l = oracle_verify(b)
     compare_attention(out, lse, ref_o, ref_l, rows_of(b), torch.bfloat16)
+
+
+def test_lse_is_optional():
+    """lse may be NULL: the outputs are bit-identical to a run that writes it, for the
+    verification kernel with pairs split over several CTAs (the merge reads the pieces'
+    statistics from the workspace, not from lse) and for the dedicated prefill kernel."""
+    b = wl.make_batch("budget8n_bf16", seed=21, n=4, lengths=[16, 3, 9, 1],
+                      ctx_lengths=[3000, 700, 0, 5000], hq=8, hkv=2, d=128, poison=True)
+    bd = to_dev(b)
+    out1, lse1 = gpu_verify(bd)
+    ws = svp.Workspace(svp.verify_attn_workspace_size(bd.n, bd.m_cap, bd.W, bd.hq, bd.hkv, bd.d,
+                                                      bd.q.dtype, svp.TILE_AUTO))
+    out2, lse2 = svp.verify_attn_packed(bd.q, bd.k_new, bd.v_new, bd.ctx_len, bd.cu_slots, w=bd.W,
+                                        k_ctx=bd.k_ctx, v_ctx=bd.v_ctx, cu_ctx=bd.cu_ctx,
+                                        want_lse=False, ws=ws)
+    torch.cuda.synchronize()
+    assert lse2 is None and ws.read_status() == 0
+    assert torch.equal(out1[:b.m_live], out2[:b.m_live])
+    q, k, v = wl.make_prefill(seed=3, s=500, hq=4, hkv=2, d=128)
+    cu = torch.tensor([0, 500], dtype=torch.int32).cuda()
+    p1, l1 = svp.prefill_attn(q.cuda(), k.cuda(), v.cuda(), cu, max_s=500)
+    p2, l2 = svp.prefill_attn(q.cuda(), k.cuda(), v.cuda(), cu, max_s=500, want_lse=False)
+    torch.cuda.synchronize()
+    assert l2 is None and torch.equal(p1, p2)
