@@ -222,3 +222,40 @@ def test_margin_workspace_returns_to_zero_and_serves_any_size():
         assert np.array_equal(outs[5].cpu().numpy(), nxt)
         assert ws.read_status() == 0
         assert int(ws.buf[256:].to(torch.int32).sum()) == 0
+
+
+def test_null_outputs_through_the_abi():
+    """Any output pointer of svp_draft_margin / svp_margin_accept may be NULL (called
+    through the C ABI directly; the binding always passes all of them): the outputs that are
+    given equal those of a call that writes everything, and the NULL ones are skipped."""
+    import ctypes
+    L = svp.lib()
+    g = torch.Generator().manual_seed(17)
+    rows, V = 40, 32000
+    z = (torch.randn(rows, V, generator=g) * 2).to(torch.bfloat16).cuda()
+    full = svp.draft_margin(z)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream().cuda_stream
+    ws = svp.Workspace(svp.draft_margin_workspace_size(rows, V))
+    for keep in range(4):
+        outs = [torch.full((rows,), -5, dtype=torch.int32 if i == 0 else torch.float32, device="cuda")
+                for i in range(4)]
+        ptrs = [outs[i].data_ptr() if i == keep else None for i in range(4)]
+        rc = L.svp_draft_margin(z.data_ptr(), V, rows, V, svp.SVP_BF16, *ptrs, ws.ptr, ws.nbytes, st)
+        assert rc == svp.SVP_OK
+        torch.cuda.synchronize()
+        assert torch.equal(outs[keep], full[keep])
+    # fused: only the per-request results
+    n = 5
+    cu = torch.tensor([0, 8, 8, 15, 31, 40], dtype=torch.int32).cuda()
+    tok = torch.randint(0, V, (rows,), generator=g, dtype=torch.int32).cuda()
+    ref = svp.margin_accept(z, tok, cu)
+    torch.cuda.synchronize()
+    acc = torch.full((n,), -5, dtype=torch.int32, device="cuda")
+    nxt = torch.full((n,), -5, dtype=torch.int32, device="cuda")
+    wsa = svp.Workspace(svp.margin_accept_workspace_size(n, rows, V))
+    rc = L.svp_margin_accept(z.data_ptr(), V, rows, V, svp.SVP_BF16, tok.data_ptr(), cu.data_ptr(), n,
+                             None, None, None, None, acc.data_ptr(), nxt.data_ptr(), wsa.ptr, wsa.nbytes, st)
+    assert rc == svp.SVP_OK
+    torch.cuda.synchronize()
+    assert torch.equal(acc, ref[4]) and torch.equal(nxt, ref[5])

@@ -259,3 +259,18 @@ def test_workspace_reused_across_sizes():
             if acc[i] != o_acc[i] or nxt[i] != o_nxt[i]:
                 assert _borderline(zf, tok, cu, 1.0, ua, un, i, int(nxt[i])), (n, V, i)
         assert torch.count_nonzero(ws.buf[256:]).item() == 0   # all zero again past the header
+
+
+def test_p_draft_is_optional():
+    """p_draft may be NULL: accept_len and next_token equal those of a call that writes it."""
+    n, V = 10, 5000
+    z, zf, tok, cu, ua, un = _batch(71, n, V, torch.bfloat16)
+    d = lambda a: torch.from_numpy(np.asarray(a)).cuda()
+    args = (z.cuda(), d(tok), d(cu), d(ua), d(un))
+    acc1, nxt1, pd1 = svp.stochastic_accept(*args, temperature=0.9)
+    outs = (torch.full((n,), -5, dtype=torch.int32, device="cuda"),
+            torch.full((n,), -5, dtype=torch.int32, device="cuda"), None)
+    acc2, nxt2, pd2 = svp.stochastic_accept(*args, temperature=0.9, outs=outs)
+    torch.cuda.synchronize()
+    assert pd2 is None
+    assert torch.equal(acc1, acc2) and torch.equal(nxt1, nxt2)
