@@ -102,3 +102,59 @@ def test_binding_refuses_cpu_tensors():
                                torch.tensor([0, 4], dtype=torch.int32), w=16,
                                k_ctx=q[:0, :1], v_ctx=q[:0, :1],
                                cu_ctx=torch.zeros(2, dtype=torch.int64))
+
+
+def test_host_checks_of_the_logit_and_allocator_calls(L):
+    """The stochastic verifier, draft features, ACT truncation, the DVL allocator, greedy
+    accept and both fused margin calls reject bad arguments (and empty calls return OK)
+    on the host, before any CUDA call."""
+    OK, INV, UNS, WSP = svp.SVP_OK, svp.SVP_EINVAL, svp.SVP_EUNSUPPORTED, svp.SVP_EWORKSPACE
+    big = 1 << 30
+    nb = ctypes.c_size_t(0)
+    # stochastic prefix verifier
+    assert L.svp_stochastic_accept_workspace_size(224, 1, ctypes.byref(nb)) == INV     # vocab < 2
+    assert L.svp_stochastic_accept_workspace_size(224, 248320, ctypes.byref(nb)) == OK
+    need = nb.value
+    st = lambda T=1.0, vocab=1000, stride=1000, dtype=1, ws=1, wsb=big, n=4, logits=1: \
+        L.svp_stochastic_accept(logits, stride, 16, vocab, dtype, 1, 1, n, T, 1, 1, 1, 1, None, ws, wsb, None)
+    assert st(T=0.0) == INV and st(T=-1.0) == INV and st(T=float("nan")) == INV
+    assert st(logits=None) == INV and st(vocab=1) == INV and st(stride=999) == INV
+    assert st(ws=None) == INV and st(n=-1) == INV
+    assert st(dtype=7) == UNS
+    assert st(wsb=16) == WSP
+    assert st(n=0) == OK                                                              # nothing to do
+    assert need > 0
+    # draft features
+    assert L.svp_draft_features_workspace_size(8, 15, ctypes.byref(nb)) == INV          # vocab < 16
+    ft = lambda rows=8, vocab=1000, stride=1000, dtype=1, wsb=big, out=1: \
+        L.svp_draft_features(1, stride, rows, vocab, dtype, out, 1, wsb, None)
+    assert ft(vocab=15) == INV and ft(rows=-1) == INV and ft(stride=999) == INV and ft(out=None) == INV
+    assert ft(dtype=7) == UNS and ft(wsb=16) == WSP and ft(rows=0) == OK
+    # ACT truncation
+    assert L.svp_act_truncate(1, 1, 4, 0, 0.5, 1, None) == INV                         # w < 1
+    assert L.svp_act_truncate(1, 0, 4, 8, 0.5, 1, None) == INV                         # stride < 1
+    assert L.svp_act_truncate(None, 1, 4, 8, 0.5, 1, None) == INV
+    assert L.svp_act_truncate(1, 1, 0, 8, 0.5, 1, None) == OK
+    # DVL allocator / packer
+    dv = lambda n_bs=8, w=16, per=8, m_cap=128, wsb=256, scores=1: L.svp_dvl_allocate_pack(
+        scores, n_bs, w, None, per, None, None, None, m_cap, 0, 0, -1, None, 1, 1, None, None, None,
+        None, 1, wsb, None)
+    assert dv(scores=None) == INV and dv(n_bs=0) == INV and dv(w=1) == INV and dv(per=17) == INV
+    assert dv(per=0) == INV and dv(m_cap=0) == INV
+    assert dv(n_bs=4096) == UNS and dv(w=17, per=8) == UNS
+    assert dv(wsb=16) == WSP
+    # greedy accept and the fused margin calls
+    assert L.svp_greedy_accept(1, 1, 1, -1, 8, 1, 1, None) == INV
+    assert L.svp_greedy_accept(None, 1, 1, 4, 8, 1, 1, None) == INV
+    assert L.svp_greedy_accept(1, 1, 1, 0, 8, 1, 1, None) == OK
+    assert L.svp_margin_accept(1, 1000, 16, 1000, 1, 1, None, 4, None, None, None, None, 1, 1, 1, big,
+                               None) == INV                                           # no cu_slots
+    na = L.svp_margin_accept_noalloc
+    na.restype = ctypes.c_int
+    na.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32] + [ctypes.c_void_p] * 7
+    assert na(1, 1000, 16, 1000, 1, 1, None, 4, None, None, None, None, 1, 1, None) == INV
+    # sizes whose workspace exceeds the fixed 2 MiB scratch (8192 rows of V = 248,320)
+    assert L.svp_margin_accept_workspace_size(512, 8192, 248320, ctypes.byref(nb)) == OK
+    assert nb.value > (2 << 20)
+    assert na(1, 248320, 8192, 248320, 1, 1, 1, 512, None, None, None, None, 1, 1, None) == WSP
