@@ -66,6 +66,7 @@ struct VtRows {
     int32_t req_ctx[kReqCache];   // contiguous context: first token row (< 2^31, host-checked)
     int32_t pslot[256];   // merge: partial slot of each piece (pieces <= CTAs <= 256)
     int32_t npend;        // merges this CTA owes (it delivered the last piece of a pair)
+    uint32_t v_seen;      // tiles whose V fill the PV issuer has seen land (S issuer reads it)
     int32_t pend[2][8];   // pair, cf, cl, nact, out_row0, hg, u_pair0 (lo, hi)
 };
 
@@ -309,11 +310,40 @@ struct RingPos {
 __device__ __forceinline__ RingPos ring_add(RingPos r, uint32_t n, uint32_t nslot)
 {
     r.slot += n;
-    while (r.slot >= nslot) {
+    while (nslot != 0 && r.slot >= nslot) {   // (a ring always has slots; never spin on 0)
         r.slot -= nslot;
         r.phase ^= 1u;
     }
     return r;
+}
+
+// Bounded wait until a shared-memory counter that another warp of the CTA advances reaches
+// need; the fences pair with the writer's, so what the writer had observed before its store
+// (here: an mbarrier phase that completed) is observed by the caller after it returns.
+__device__ __forceinline__ bool vt_wait_count(const uint32_t *cnt, uint32_t need,
+                                              volatile int *abort_flag)
+{
+    const volatile uint32_t *c = cnt;
+    if (*c >= need) {
+        __threadfence_block();
+        return true;
+    }
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(64);
+        if (*c >= need) {
+            __threadfence_block();
+            return true;
+        }
+        if ((i & 15u) == 0) {
+            if (*abort_flag)
+                return false;
+            if ((int64_t)(global_ns() - t0) > (int64_t)kWaitLimitNs) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
 }
 
 // One merge pass over NB partial slabs staged in shared memory: column block h (128 columns
@@ -446,6 +476,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         rs->flag[0] = rs->flag[1] = 0;
         rs->rescale = 0;
         rs->npend = 0;
+        rs->v_seen = 0;
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tm_q);
@@ -683,6 +714,25 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     const int b = it & 1;
                     if (!(ok = mbar_wait(bar_sfree(b), ((it >> 1) & 1) ^ 1, abort_flag)))
                         break;
+                    // K(it) half h goes into the slot whose previous fill was ring position
+                    // pos - nslot.  When that fill was a V half (an odd slot count at
+                    // d = 128), only the PV issuer has waited on it, and a parity wait here
+                    // cannot tell "that V fill still in flight" from "this K fill landed"
+                    // (both leave the barrier one phase short of, or at, the same parity).
+                    // So first wait until the PV issuer has seen that V fill land; in the
+                    // steady state it has (S(it) follows the softmax of it - 2, which
+                    // follows PV's wait for the earlier tile's V).
+                    uint32_t need = 0;
+                    for (int h = 0; h < DH; ++h) {
+                        const uint32_t pos = it * 2u * DH + (uint32_t)h;
+                        if (pos >= (uint32_t)nslot) {
+                            const uint32_t prev = pos - (uint32_t)nslot;
+                            if (prev % (2u * DH) >= (uint32_t)DH)
+                                need = max(need, prev / (2u * DH) + 1u);
+                        }
+                    }
+                    if (need > 0 && !(ok = vt_wait_count(&rs->v_seen, need, abort_flag)))
+                        break;
                     for (int h = 0; h < DH && ok; ++h) {
                         const RingPos q = ring_add(kpos, (uint32_t)h, (uint32_t)nslot);
                         ok = mbar_wait(bar_full(q.slot), q.phase, abort_flag);
@@ -786,6 +836,9 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     }
                     if (!ok)
                         break;
+                    // V(it) has landed: the S issuer may reuse the parity of its slots
+                    __threadfence_block();
+                    *reinterpret_cast<volatile uint32_t *>(&rs->v_seen) = it + 1u;
                     tc_fence_after();
                     const int32_t kv = vt_kvalid(p, s, s.t0 + k, L, k_i);
                     const int32_t k16 = (kv + 15) / 16;
