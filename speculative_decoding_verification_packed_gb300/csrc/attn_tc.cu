@@ -747,13 +747,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
 
     // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // read once every role has finished, so that a wait given up late is reported too
     if (*abort_flag && tid == 0) {
         set_status(p.status, SVP_DEV_TIMEOUT);
         *reinterpret_cast<volatile int32_t *>(p.status + kWsPoisonWord) = 1;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     if (warp == 1)
         tmem_dealloc(tmem, C::TMEM_COLS);
 }

@@ -501,11 +501,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
         }
     }
 
-    if (*abort_flag && tid == 0)
-        set_status(p.status, SVP_DEV_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // read once every role has finished, so that a wait given up late is reported too
+    if (*abort_flag && tid == 0)
+        set_status(p.status, SVP_DEV_TIMEOUT);
     if (warp == 1) {
         __syncwarp();
         tmem_dealloc(tmem, 512);

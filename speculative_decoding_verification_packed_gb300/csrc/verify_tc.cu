@@ -1096,10 +1096,12 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                 if (kvalid < k16 && t >= kvalid && t < k16) {
                     for (int h = 0; h < DH; ++h) {
                         const uint32_t sq = it * 2 * DH + DH + h;
-                        if (!mbar_wait(bar_full(sq % nslot), (sq / nslot) & 1, abort_flag)) {
-                            ok = false;
+                        // only some threads wait here, after the tile's last collective
+                        // decision: a failed wait (the abort flag is set by then) does not
+                        // touch ok, so the four warps still leave the loops together; the
+                        // other roles give up at their next wait and the launch reports it
+                        if (!mbar_wait(bar_full(sq % nslot), (sq / nslot) & 1, abort_flag))
                             break;
-                        }
                         const uint32_t vrow = sbase + p.off_ring + (sq % nslot) * kSlotBytes + t * 128;
                         for (int c = 0; c < 2; ++c)
                             for (int v = 0; v < 8; ++v)
@@ -1331,13 +1333,15 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
         }
     }
 
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // read once every role has finished, so that a wait given up late (in a merge, say) is
+    // reported too and the workspace is marked for clearing
     if (*abort_flag && tid == 0) {
         set_status(p.status, SVP_DEV_TIMEOUT);
         *reinterpret_cast<volatile int32_t *>(p.status + kWsPoisonWord) = 1;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     if (warp == 1)
         tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
 }
