@@ -1323,6 +1323,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_tc_kernel(const __grid_co
                     if (!last_pass)
                         __threadfence_block();
                 }
+                // landed is per thread (with the abort flag set, a thread may see the slabs
+                // land or give up): decide together, so that the loop test below is the
+                // same in all four warps
+                if (named_bar_any(1, 128, !ok))
+                    ok = false;
             }
             if (named_bar_any(1, 128, !ok)) {
                 ok = false;
