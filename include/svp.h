@@ -232,6 +232,21 @@ svp_status svp_greedy_accept(const int32_t *target_argmax, const int32_t *tokens
 svp_status svp_margin_accept_workspace_size(int32_t n, int32_t m_cap, int32_t vocab,
                                             size_t *bytes);
 
+/*
+ * logits [m_cap, row_stride] (dtype F32 or BF16, else SVP_EUNSUPPORTED): packed target
+ * rows, row off_i + j the target distribution after slot j of request i; 2 <= vocab <=
+ * row_stride.  tokens [m_cap] int32 (row off_i = anchor, off_i + j = draft j) and
+ * cu_slots [n+1] as for svp_greedy_accept.  Outputs: top1_idx / top1 / top2 / margin
+ * [m_cap] as svp_draft_margin for the live rows r < cu_slots[n] (other rows are neither
+ * read nor written; any of the four pointers may be NULL); accept_len / next_token [n]
+ * as svp_greedy_accept (required).  ws: at least svp_margin_accept_workspace_size bytes,
+ * zeroed once by svp_workspace_init; every call leaves it zeroed.  A NULL cu_slots,
+ * tokens, accept_len or next_token, n < 0, vocab < 2 or row_stride < vocab returns
+ * SVP_EINVAL; a missing or small workspace SVP_EWORKSPACE; nothing is enqueued then.
+ * cu_slots that break the contract on the device (not starting at 0, decreasing, or
+ * cu_slots[n] > m_cap): no logit is read, no output is written and SVP_DEV_BAD_SLOTS is
+ * set in the status word.
+ */
 svp_status svp_margin_accept(const void *logits, int64_t row_stride, int32_t m_cap,
                              int32_t vocab, svp_dtype dtype, const int32_t *tokens,
                              const int32_t *cu_slots, int32_t n, int32_t *top1_idx,

@@ -149,6 +149,15 @@ def test_host_checks_of_the_logit_and_allocator_calls(L):
     assert L.svp_greedy_accept(1, 1, 1, 0, 8, 1, 1, None) == OK
     assert L.svp_margin_accept(1, 1000, 16, 1000, 1, 1, None, 4, None, None, None, None, 1, 1, 1, big,
                                None) == INV                                           # no cu_slots
+    # every call below breaks one documented rule, so none reaches a CUDA call
+    ma = lambda logits=1, stride=1000, rows=16, vocab=1000, dtype=1, tokens=1, n=4, acc=1, nxt=1, \
+        ws=1, wsb=big: L.svp_margin_accept(logits, stride, rows, vocab, dtype, tokens, 1, n, None, None,
+                                           None, None, acc, nxt, ws, wsb, None)
+    assert ma(tokens=None) == INV and ma(acc=None) == INV and ma(nxt=None) == INV
+    assert ma(n=-1) == INV and ma(vocab=1) == INV and ma(stride=999) == INV and ma(rows=-1) == INV
+    assert ma(logits=None) == INV
+    assert ma(dtype=7) == UNS
+    assert ma(ws=None) == WSP and ma(wsb=16) == WSP
     na = L.svp_margin_accept_noalloc
     na.restype = ctypes.c_int
     na.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
