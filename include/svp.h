@@ -322,8 +322,9 @@ svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, int32_t w,
 
 /*
  * src [src_rows, row_bytes] and dst [rows, row_bytes] device buffers, 16-byte aligned,
- * row_bytes a multiple of 16 (SVP_EUNSUPPORTED otherwise); idx [rows] int32 (e.g. the
- * packed KV references of svp_dvl_allocate_pack).  No workspace.
+ * row_bytes >= 16 (SVP_EINVAL otherwise, as for NULL pointers or negative counts) and a
+ * multiple of 16 (SVP_EUNSUPPORTED otherwise, as for unaligned buffers); idx [rows] int32
+ * (e.g. the packed KV references of svp_dvl_allocate_pack).  No workspace.
  */
 svp_status svp_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes,
                            const int32_t *idx, int32_t rows, void *dst, void *stream);
@@ -332,9 +333,9 @@ svp_status svp_gather_rows(const void *src, int64_t src_rows, int64_t row_bytes,
  * The same for up to SVP_GATHER_MAX_FIELDS fields that share one row map, in one launch
  * (a step packs its query, key, value and logit rows together).  fields: a HOST array of
  * n_fields descriptors (1 <= n_fields <= SVP_GATHER_MAX_FIELDS), read during the call and
- * not retained; each src / dst pair follows the rules of svp_gather_rows (16-byte aligned,
- * row_bytes a multiple of 16, SVP_EUNSUPPORTED otherwise); dst of field f holds
- * [rows, row_bytes_f].  idx [rows] int32, shared.  No workspace.
+ * not retained, SVP_EINVAL for a count outside that range; each src / dst pair follows
+ * the rules of svp_gather_rows (16-byte aligned, row_bytes >= 16 and a multiple of 16);
+ * dst of field f holds [rows, row_bytes_f].  idx [rows] int32, shared.  No workspace.
  */
 #define SVP_GATHER_MAX_FIELDS 8
 typedef struct {
