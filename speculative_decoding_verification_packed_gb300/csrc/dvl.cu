@@ -336,12 +336,12 @@ extern "C" svp_status svp_dvl_allocate_pack(const float *scores, int32_t n_bs, i
                                             void *stream)
 {
     using namespace svp;
-    if (!scores || !k_out || !cu_slots || !ws || n_bs < 1 || w < 2 || m_cap < 1 ||
+    if (!scores || !k_out || !cu_slots || n_bs < 1 || w < 2 || m_cap < 1 ||
         budget_per_req < 1 || budget_per_req > w)
         return SVP_EINVAL;
     if (n_bs > kDvlMaxRequests || w > kDvlMaxW)
         return SVP_EUNSUPPORTED;
-    if (ws_bytes < kWsHeader)
+    if (!ws || ws_bytes < kWsHeader)
         return SVP_EWORKSPACE;
     static std::atomic<uint64_t> configured{0};
     if (set_smem_limit_once(dvl_kernel, (int)sizeof(DvlShared), configured) != cudaSuccess)

@@ -691,14 +691,14 @@ extern "C" svp_status svp_draft_features(const void *logits, int64_t row_stride,
                                          void *ws, size_t ws_bytes, void *stream)
 {
     using namespace svp;
-    if (!logits || !features || !ws || rows < 0 || vocab < kFtTop || row_stride < vocab)
+    if (!logits || !features || rows < 0 || vocab < kFtTop || row_stride < vocab)
         return SVP_EINVAL;
     if (dtype != SVP_BF16 && dtype != SVP_F32)
         return SVP_EUNSUPPORTED;
     FtParams p;
     size_t off_tk, off_part, need;
     ft_plan(rows, vocab, off_tk, off_part, need);
-    if (ws_bytes < need)
+    if (!ws || ws_bytes < need)
         return SVP_EWORKSPACE;
     if (rows == 0)
         return SVP_OK;

@@ -592,7 +592,7 @@ extern "C" svp_status svp_stochastic_accept(const void *logits, int64_t row_stri
 {
     using namespace svp;
     if (!logits || !tokens || !cu_slots || !u_accept || !u_next || !accept_len ||
-        !next_token || !ws || n < 0 || m_cap < 0 || vocab < 2 || row_stride < vocab ||
+        !next_token || n < 0 || m_cap < 0 || vocab < 2 || row_stride < vocab ||
         !(temperature > 0.0f))
         return SVP_EINVAL;
     if (dtype != SVP_BF16 && dtype != SVP_F32)
@@ -600,7 +600,7 @@ extern "C" svp_status svp_stochastic_accept(const void *logits, int64_t row_stri
     StParams p;
     size_t off_stat, off_tk, off_part, need;
     st_plan(m_cap, vocab, off_stat, off_tk, off_part, need);
-    if (ws_bytes < need)
+    if (!ws || ws_bytes < need)
         return SVP_EWORKSPACE;
     if (n == 0)
         return SVP_OK;

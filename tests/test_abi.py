@@ -119,30 +119,30 @@ def test_host_checks_of_the_logit_and_allocator_calls(L):
         L.svp_stochastic_accept(logits, stride, 16, vocab, dtype, 1, 1, n, T, 1, 1, 1, 1, None, ws, wsb, None)
     assert st(T=0.0) == INV and st(T=-1.0) == INV and st(T=float("nan")) == INV
     assert st(logits=None) == INV and st(vocab=1) == INV and st(stride=999) == INV
-    assert st(ws=None) == INV and st(n=-1) == INV
+    assert st(ws=None) == WSP and st(n=-1) == INV
     assert st(dtype=7) == UNS
     assert st(wsb=16) == WSP
     assert st(n=0) == OK                                                              # nothing to do
     assert need > 0
     # draft features
     assert L.svp_draft_features_workspace_size(8, 15, ctypes.byref(nb)) == INV          # vocab < 16
-    ft = lambda rows=8, vocab=1000, stride=1000, dtype=1, wsb=big, out=1: \
-        L.svp_draft_features(1, stride, rows, vocab, dtype, out, 1, wsb, None)
+    ft = lambda rows=8, vocab=1000, stride=1000, dtype=1, ws=1, wsb=big, out=1: \
+        L.svp_draft_features(1, stride, rows, vocab, dtype, out, ws, wsb, None)
     assert ft(vocab=15) == INV and ft(rows=-1) == INV and ft(stride=999) == INV and ft(out=None) == INV
-    assert ft(dtype=7) == UNS and ft(wsb=16) == WSP and ft(rows=0) == OK
+    assert ft(dtype=7) == UNS and ft(wsb=16) == WSP and ft(ws=None) == WSP and ft(rows=0) == OK
     # ACT truncation
     assert L.svp_act_truncate(1, 1, 4, 0, 0.5, 1, None) == INV                         # w < 1
     assert L.svp_act_truncate(1, 0, 4, 8, 0.5, 1, None) == INV                         # stride < 1
     assert L.svp_act_truncate(None, 1, 4, 8, 0.5, 1, None) == INV
     assert L.svp_act_truncate(1, 1, 0, 8, 0.5, 1, None) == OK
     # DVL allocator / packer
-    dv = lambda n_bs=8, w=16, per=8, m_cap=128, wsb=256, scores=1: L.svp_dvl_allocate_pack(
+    dv = lambda n_bs=8, w=16, per=8, m_cap=128, ws=1, wsb=256, scores=1: L.svp_dvl_allocate_pack(
         scores, n_bs, w, None, per, None, None, None, m_cap, 0, 0, -1, None, 1, 1, None, None, None,
-        None, 1, wsb, None)
+        None, ws, wsb, None)
     assert dv(scores=None) == INV and dv(n_bs=0) == INV and dv(w=1) == INV and dv(per=17) == INV
     assert dv(per=0) == INV and dv(m_cap=0) == INV
     assert dv(n_bs=4096) == UNS and dv(w=17, per=8) == UNS
-    assert dv(wsb=16) == WSP
+    assert dv(wsb=16) == WSP and dv(ws=None) == WSP
     # greedy accept and the fused margin calls
     assert L.svp_greedy_accept(1, 1, 1, -1, 8, 1, 1, None) == INV
     assert L.svp_greedy_accept(None, 1, 1, 4, 8, 1, 1, None) == INV
